@@ -1,0 +1,366 @@
+/*
+ * CPU oracle for the batched speculative-sampling verifier.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header or constant table with the
+ * CUDA library; the one thing both sides agree on is the written definition
+ * of the counter-based generator below, which each side implements on its own.
+ *
+ * Plain, slow and single-threaded, in double precision, one request at a time,
+ * in the order the pages state the method:
+ *
+ *   [P3] bloss0m, "Speculative Decoding：用小模型打草稿、大模型一次驗…"
+ *        - "Speculative sampling (Section 2.3)": propose x ~ q, keep it when
+ *          q(x) <= p(x), otherwise reject with probability 1 - p(x)/q(x) and
+ *          redraw from p' = norm(max(0, p - q)).
+ *        - "Algorithm 1": n = number of drafts accepted before the first
+ *          rejection; the extra token t comes from the adjusted p_{n+1} when
+ *          n < gamma, else from p_{gamma+1}; output x_1..x_n, t.
+ *        - Theorem 3.5 / Corollary 3.6: beta = sum_x min(p(x), q(x)).
+ *   [P4] vllbc, "Speculative Decoding：draft 先猜，target 一次验证"
+ *        - Algorithm 1 steps 3-4 (accept test, recover / bonus token).
+ *        - Section 2.2 note: argmax / temperature fold into the adjusted p, q.
+ *   [P2] timinsight, "Speculative Decoding 實作指南：基準、驗證與取捨"
+ *        - Step 2 verification pseudo-code: softmax of the target logits, the
+ *          strict test u < min(1, p/q), break at the first rejection, the
+ *          residual clamp(p - q, 0) and the fallback to p when it sums to ~0.
+ *   [P1] tarrragon, speculative decoding tag page, "演算法核心：sampling 階段
+ *        的接受邏輯": the same loop, strict `<`, bonus token when all accepted.
+ *
+ * Readings where the pages leave a step open (each is listed with its reason in
+ * the design notes of the repository):
+ *   - the accept test is strict: r < min(1, p/q)  ([P1], [P2]);
+ *   - p(x) = 0 gives ratio 0 (reject); q(x) = 0 < p(x) gives ratio +inf (accept);
+ *   - the zero-residual fallback of [P2] is taken exactly: only when every
+ *     max(0, p - q) is 0 does the correction draw from p instead;
+ *   - temperature divides the target logits only; draft probabilities arrive
+ *     already adjusted;
+ *   - the correction / bonus draw is the exponential race
+ *     argmax_v w(v) / E_v with E_v = -ln U_v, an exact sampler of norm(w):
+ *     E_v / w(v) is exponential with rate w(v) and the smallest of independent
+ *     exponentials falls on v with probability w(v) / sum(w);
+ *   - T == 0 is greedy: g_i = argmax of row i (lowest index on ties), accept
+ *     iff x_i == g_i, beta_i = [x_i == g_i], t = g_n;
+ *   - beta is emitted for every draft position, also after the first reject;
+ *   - a draft id outside [0, V) is treated as rejected with p(x) = q(x) = 0 and
+ *     the call reports ORACLE_BAD_DRAFT_ID.
+ *
+ * Counter-based generator (the pages only say "uniform random"): SplitMix64
+ * (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+ * OOPSLA 2014; the finaliser as published by Vigna) keyed by
+ *     k = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream)),  h = sm(k ^ v),
+ *     U = ((h >> 41) + 0.5) * 2^-23    (23 bits, strictly inside (0, 1)).
+ * stream 0 / v 0 is the accept uniform r_i of draft position pos; stream 1 / v
+ * is the race uniform of vocabulary entry v at output position pos.  U equals
+ * (2k+1) 2^-24 with 2k+1 < 2^24, an exact float and an exact double, so both
+ * sides see the same number.
+ *
+ * Near ties (inputs on which a float32 implementation may legitimately decide
+ * differently from this double-precision one) are flagged per request:
+ *   - an accept test with |r - min(1, ratio)| <= 1e-5 * max(r, min(1, ratio))
+ *     at a tested position (0..n, or all positions when n == gamma);
+ *   - a race whose two best keys k1 >= k2 satisfy k1 - k2 <= 1e-5 * k1.
+ *
+ * Parity pins (tests, CPU only): the splitmix64 published output for seed 0,
+ * uniformity of U, softmax closed forms, beta by hand on tiny rows and its
+ * identities, output distribution == p by chi-square over 1e6 draws, accept
+ * rate vs beta within 3 sigma, Eq. (1) for i.i.d. positions, the p == q and
+ * disjoint-support special cases, at least one token per step, greedy argmax
+ * against brute force with planted ties.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_INVALID_ARG (-1)
+#define ORACLE_UNSUPPORTED_DTYPE (-2)
+#define ORACLE_OOM (-4)
+#define ORACLE_BAD_DRAFT_ID (-5)
+
+#define ORACLE_DTYPE_F32 0
+#define ORACLE_DTYPE_BF16 1
+
+#define NEAR_TIE_REL 1e-5
+
+/* ---------------------------------------------------------------------- */
+/* Counter-based generator                                                */
+/* ---------------------------------------------------------------------- */
+
+uint64_t oracle_splitmix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ULL;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+uint64_t oracle_stream_key(uint64_t seed, uint64_t b, uint64_t pos, uint64_t stream) {
+  uint64_t k = oracle_splitmix64(seed);
+  k = oracle_splitmix64(k ^ b);
+  return oracle_splitmix64(k ^ ((pos << 8) | stream));
+}
+
+double oracle_uniform(uint64_t seed, uint64_t b, uint64_t pos, uint64_t stream, uint64_t v) {
+  uint64_t h = oracle_splitmix64(oracle_stream_key(seed, b, pos, stream) ^ v);
+  return ((double)(h >> 41) + 0.5) * (1.0 / 8388608.0);
+}
+
+/* Fills out[j] = U(seed, b, pos, stream, v0 + j) for j < n (used by tests). */
+void oracle_uniform_fill(uint64_t seed, uint64_t b, uint64_t pos, uint64_t stream, uint64_t v0,
+                         int64_t n, double* out) {
+  for (int64_t j = 0; j < n; ++j) out[j] = oracle_uniform(seed, b, pos, stream, v0 + (uint64_t)j);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Input access                                                           */
+/* ---------------------------------------------------------------------- */
+
+/* One stored target logit as a double.  bf16 is the top half of an IEEE
+ * binary32, so widening it is exact. */
+static double logit_at(const void* base, int dtype, size_t idx) {
+  if (dtype == ORACLE_DTYPE_F32) return (double)((const float*)base)[idx];
+  uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* p(v) = exp((L(v) - max L) / T) / sum_u exp((L(u) - max L) / T): the target
+ * softmax at temperature T ([P2] Step 2 pseudo-code applies softmax to the
+ * target logits; [P4] Section 2.2 folds temperature into the adjusted p). */
+static void softmax_row(const void* logits, int dtype, size_t row, int V, double T, double* p) {
+  double mx = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double l = logit_at(logits, dtype, row * (size_t)V + (size_t)v);
+    if (l > mx) mx = l;
+  }
+  double sum = 0.0;
+  for (int v = 0; v < V; ++v) {
+    p[v] = exp((logit_at(logits, dtype, row * (size_t)V + (size_t)v) - mx) / T);
+    sum += p[v];
+  }
+  for (int v = 0; v < V; ++v) p[v] /= sum;
+}
+
+/* Greedy target token: first index of the largest stored value. */
+static int argmax_row(const void* logits, int dtype, size_t row, int V) {
+  int best = 0;
+  double bv = logit_at(logits, dtype, row * (size_t)V);
+  for (int v = 1; v < V; ++v) {
+    double l = logit_at(logits, dtype, row * (size_t)V + (size_t)v);
+    if (l > bv) {
+      bv = l;
+      best = v;
+    }
+  }
+  return best;
+}
+
+/* ---------------------------------------------------------------------- */
+/* One request                                                            */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * Verifies one request b with gamma drafts.
+ *   tgt    : the request's gamma+1 target logit rows, row-major [gamma+1, V]
+ *   draft  : the request's gamma draft probability rows [gamma, V] (ignored, and
+ *            may be NULL, when T == 0)
+ *   ids    : the gamma draft token ids
+ * Outputs (any may be NULL):
+ *   tokens [gamma+1]  accepted drafts, then the correction / bonus token, then -1
+ *   num_accepted [1]  n
+ *   beta [gamma]      sum_v min(p_i(v), q_i(v))
+ *   p_x, q_x [gamma]  p_i(x_i), q_i(x_i)
+ *   accept [gamma]    the accept test at every position (also after the first
+ *                     rejection, where it no longer affects the output)
+ *   pos_near_tie [gamma]  accept-test near tie at that position
+ *   near_tie [1]      request-level flag (tested positions or the race)
+ * Returns ORACLE_OK, ORACLE_BAD_DRAFT_ID or ORACLE_OOM.
+ */
+int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, const float* draft,
+                          const int32_t* ids, int V, double T, uint64_t seed, int32_t* tokens,
+                          int32_t* num_accepted, double* beta, double* p_x, double* q_x,
+                          int32_t* accept, int32_t* pos_near_tie, int32_t* near_tie) {
+  int status = ORACLE_OK;
+  int n = gamma;
+  int req_tie = 0;
+  int* acc = (int*)calloc((size_t)(gamma > 0 ? gamma : 1), sizeof(int));
+  int* tie = (int*)calloc((size_t)(gamma > 0 ? gamma : 1), sizeof(int));
+  if (!acc || !tie) {
+    free(acc);
+    free(tie);
+    return ORACLE_OOM;
+  }
+  int t = -1;
+
+  if (T == 0.0) {
+    /* Greedy: the adjusted p and q of [P4] Section 2.2 are one-hot at the
+     * target argmax and at the draft id. */
+    int* g = (int*)malloc(sizeof(int) * (size_t)(gamma + 1));
+    if (!g) {
+      free(acc);
+      free(tie);
+      return ORACLE_OOM;
+    }
+    for (int i = 0; i <= gamma; ++i) g[i] = argmax_row(tgt, dtype, (size_t)i, V);
+    for (int i = 0; i < gamma; ++i) {
+      int x = ids[i];
+      if (x < 0 || x >= V) status = ORACLE_BAD_DRAFT_ID;
+      acc[i] = (x == g[i]);
+      if (beta) beta[i] = acc[i] ? 1.0 : 0.0;
+      if (p_x) p_x[i] = acc[i] ? 1.0 : 0.0;
+      if (q_x) q_x[i] = 1.0;
+    }
+    for (int i = 0; i < gamma; ++i)
+      if (!acc[i]) {
+        n = i;
+        break;
+      }
+    t = g[n];
+    free(g);
+  } else {
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!p) {
+      free(acc);
+      free(tie);
+      return ORACLE_OOM;
+    }
+    /* Accept test and beta at every draft position. */
+    for (int i = 0; i < gamma; ++i) {
+      const float* q = draft + (size_t)i * (size_t)V;
+      softmax_row(tgt, dtype, (size_t)i, V, T, p);
+      int x = ids[i];
+      double px = 0.0, qx = 0.0;
+      if (x >= 0 && x < V) {
+        px = p[x];
+        qx = (double)q[x];
+      } else {
+        status = ORACLE_BAD_DRAFT_ID;
+      }
+      double ratio;
+      if (px == 0.0)
+        ratio = 0.0;
+      else if (qx == 0.0)
+        ratio = INFINITY;
+      else
+        ratio = px / qx;
+      double r = oracle_uniform(seed, (uint64_t)b, (uint64_t)i, 0, 0);
+      double a = ratio < 1.0 ? ratio : 1.0;
+      acc[i] = (r < a);
+      double hi = r > a ? r : a;
+      tie[i] = fabs(r - a) <= NEAR_TIE_REL * hi;
+      double s = 0.0;
+      for (int v = 0; v < V; ++v) s += (p[v] < (double)q[v]) ? p[v] : (double)q[v];
+      if (beta) beta[i] = s;
+      if (p_x) p_x[i] = px;
+      if (q_x) q_x[i] = qx;
+    }
+    for (int i = 0; i < gamma; ++i)
+      if (!acc[i]) {
+        n = i;
+        break;
+      }
+    for (int i = 0; i < gamma && i <= n; ++i) req_tie |= tie[i];
+
+    /* Correction (n < gamma) or bonus (n == gamma) distribution w. */
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!w) {
+      free(p);
+      free(acc);
+      free(tie);
+      return ORACLE_OOM;
+    }
+    softmax_row(tgt, dtype, (size_t)n, V, T, p);
+    if (n < gamma) {
+      const float* q = draft + (size_t)n * (size_t)V;
+      int any = 0;
+      for (int v = 0; v < V; ++v) {
+        double d = p[v] - (double)q[v];
+        w[v] = d > 0.0 ? d : 0.0;
+        any |= (w[v] > 0.0);
+      }
+      if (!any)
+        for (int v = 0; v < V; ++v) w[v] = p[v];
+    } else {
+      for (int v = 0; v < V; ++v) w[v] = p[v];
+    }
+    /* Exponential race: t = argmax over w(v) > 0 of w(v) / E_v, lowest v on
+     * equal keys. */
+    double k1 = -INFINITY, k2 = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+      if (!(w[v] > 0.0)) continue;
+      double e = -log(oracle_uniform(seed, (uint64_t)b, (uint64_t)n, 1, (uint64_t)v));
+      double key = w[v] / e;
+      if (key > k1) {
+        k2 = k1;
+        k1 = key;
+        t = v;
+      } else if (key > k2) {
+        k2 = key;
+      }
+    }
+    if (k2 > -INFINITY && (k1 - k2) <= NEAR_TIE_REL * k1) req_tie = 1;
+    free(w);
+    free(p);
+  }
+
+  if (tokens) {
+    for (int i = 0; i < n; ++i) tokens[i] = ids[i];
+    tokens[n] = t;
+    for (int i = n + 1; i <= gamma; ++i) tokens[i] = -1;
+  }
+  if (num_accepted) *num_accepted = n;
+  if (accept)
+    for (int i = 0; i < gamma; ++i) accept[i] = acc[i];
+  if (pos_near_tie)
+    for (int i = 0; i < gamma; ++i) pos_near_tie[i] = tie[i];
+  if (near_tie) *near_tie = req_tie;
+  free(acc);
+  free(tie);
+  return status;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Batch over a flattened ragged layout                                   */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * Ragged batch in the flattened layout of [P4] "vLLM verification path"
+ * (cu_num_draft_tokens): request b owns draft rows cu[b] .. cu[b+1]-1 and
+ * target rows cu[b]+b .. cu[b+1]+b (gamma_b + 1 rows, the last one the bonus
+ * row).  Output token slots follow the target rows.  Per-position outputs
+ * follow the draft rows; near_tie is per request.  Any output may be NULL.
+ */
+int oracle_rejection_sample(const void* target_logits, int dtype, const float* draft_probs,
+                            const int32_t* draft_ids, const int32_t* cu, int B, int V, double T,
+                            uint64_t seed, int32_t* out_tokens, int32_t* out_num_accepted,
+                            double* out_beta, double* out_p_x, double* out_q_x, int32_t* out_accept,
+                            int32_t* out_pos_near_tie, int32_t* out_near_tie) {
+  if (B <= 0 || V <= 0 || !target_logits || !draft_ids || !cu) return ORACLE_INVALID_ARG;
+  if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
+  if (!(T >= 0.0) || isinf(T)) return ORACLE_INVALID_ARG;
+  if (T > 0.0 && !draft_probs) return ORACLE_INVALID_ARG;
+  if (cu[0] != 0) return ORACLE_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (cu[b + 1] < cu[b]) return ORACLE_INVALID_ARG;
+
+  size_t esize = dtype == ORACLE_DTYPE_F32 ? 4 : 2;
+  int status = ORACLE_OK;
+  for (int b = 0; b < B; ++b) {
+    int d0 = cu[b], gamma = cu[b + 1] - cu[b];
+    size_t t0 = (size_t)d0 + (size_t)b;
+    const void* tgt = (const char*)target_logits + t0 * (size_t)V * esize;
+    const float* dr = (T > 0.0) ? draft_probs + (size_t)d0 * (size_t)V : NULL;
+    int s = oracle_verify_request(
+        b, gamma, tgt, dtype, dr, draft_ids + d0, V, T, seed, out_tokens ? out_tokens + t0 : NULL,
+        out_num_accepted ? out_num_accepted + b : NULL, out_beta ? out_beta + d0 : NULL,
+        out_p_x ? out_p_x + d0 : NULL, out_q_x ? out_q_x + d0 : NULL,
+        out_accept ? out_accept + d0 : NULL, out_pos_near_tie ? out_pos_near_tie + d0 : NULL,
+        out_near_tie ? out_near_tie + b : NULL);
+    if (s == ORACLE_OOM) return s;
+    if (s != ORACLE_OK) status = s;
+  }
+  return status;
+}

@@ -1,0 +1,171 @@
+"""Seeded synthetic inputs for the speculative-sampling verifier.
+
+This module holds none of the verifier's arithmetic: it plays the part of the
+two models that are out of scope.  The target model becomes Gaussian logits,
+the drafter becomes a softmax of those logits plus Gaussian noise (a stand-in
+for a smaller model whose distribution overlaps the target's), and the draft
+ids are drawn from the drafter's rows, exactly as Algorithm 1 draws
+x_i ~ q_i.  Tests and the benchmark build their inputs here; the CPU oracle and
+the CUDA library both receive the same tensors.
+
+Layout (the flattened ragged batch of the vLLM verification path described on
+the vllbc reading-notes page): request b has gamma_b drafts;
+cu[b+1] = cu[b] + gamma_b; draft row / id of (b, i) is cu[b] + i; target row of
+(b, i), i in [0, gamma_b], is cu[b] + b + i (the last one is the bonus row).
+
+The five standard workloads:
+  0 tiny     B=1,    gamma=4,        V=32,     f32 N(0,2^2),  q=softmax(L+N(0,0.5^2)),      T=1
+  1 small    B=8,    gamma=5,        V=32000,  f32 N(0,3^2),  q=softmax((L+N(0,1))/T),      T=1
+  2 greedy   B=64,   gamma=7,        V=128256, bf16 N(0,3^2), ids=argmax w.p. 0.75 else uniform, T=0
+  3 ragged   B=256,  gamma~U{1..8},  V=151936, f32 N(0,3^2),  q=softmax((L+N(0,1.5^2))/0.7), T=0.7
+  4 large    B=1024, gamma=7,        V=256000, bf16 N(0,3^2), q=softmax(L+N(0,1)),          T=1
+Workload k uses generator seed k and verifier seed k.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    V: int
+    dtype: str                      # "f32" or "bf16" (target logits)
+    T: float
+    seed: int                       # the verifier's generator seed
+    target_logits: torch.Tensor     # [N_t, V] float32 or bfloat16
+    draft_probs: torch.Tensor | None  # [N_d, V] float32, or None (greedy)
+    draft_ids: torch.Tensor         # [N_d] int32
+    cu: torch.Tensor                # [B+1] int32
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def n_draft(self) -> int:
+        return int(self.cu[-1])
+
+    @property
+    def n_target(self) -> int:
+        return self.n_draft + self.B
+
+    def algorithmic_bytes(self) -> int:
+        """One read of every target and draft row plus one extra target row per
+        request (the correction / bonus row)."""
+        esize = 2 if self.dtype == "bf16" else 4
+        tb = self.n_target * self.V * esize
+        db = 0 if self.draft_probs is None else self.n_draft * self.V * 4
+        extra = 0 if self.T == 0 else self.B * self.V * esize
+        return tb + db + extra
+
+    def to(self, device) -> "Workload":
+        mv = lambda t: None if t is None else t.to(device)
+        return Workload(self.name, self.B, self.V, self.dtype, self.T, self.seed,
+                        mv(self.target_logits), mv(self.draft_probs), mv(self.draft_ids),
+                        mv(self.cu), dict(self.meta))
+
+
+CONFIGS = {
+    0: dict(name="tiny B=1 gamma=4 V=32 f32 T=1", B=1, gamma=4, V=32, dtype="f32", T=1.0,
+            target_std=2.0, noise_std=0.5, draft_T=1.0, ids="sample"),
+    1: dict(name="B=8 gamma=5 V=32000 f32 T=1", B=8, gamma=5, V=32000, dtype="f32", T=1.0,
+            target_std=3.0, noise_std=1.0, draft_T=1.0, ids="sample"),
+    2: dict(name="greedy B=64 gamma=7 V=128256 bf16 T=0", B=64, gamma=7, V=128256, dtype="bf16",
+            T=0.0, target_std=3.0, noise_std=None, draft_T=None, ids="argmax0.75"),
+    3: dict(name="ragged B=256 gamma~U{1..8} V=151936 f32 T=0.7", B=256, gamma=(1, 8), V=151936,
+            dtype="f32", T=0.7, target_std=3.0, noise_std=1.5, draft_T=0.7, ids="sample"),
+    4: dict(name="large B=1024 gamma=7 V=256000 bf16 T=1", B=1024, gamma=7, V=256000, dtype="bf16",
+            T=1.0, target_std=3.0, noise_std=1.0, draft_T=1.0, ids="sample"),
+}
+
+
+def make_config(idx: int, device="cpu", B: int | None = None, V: int | None = None,
+                chunk_rows: int = 512) -> Workload:
+    """Workload ``idx`` (0..4), optionally with a smaller batch or vocabulary."""
+    c = dict(CONFIGS[idx])
+    if B is not None:
+        c["B"] = B
+    if V is not None:
+        c["V"] = V
+    name = c["name"] if (B is None and V is None) else f"{c['name']} (B={c['B']}, V={c['V']})"
+    return make_workload(name=name, B=c["B"], gamma=c["gamma"], V=c["V"], dtype=c["dtype"],
+                         T=c["T"], seed=idx, target_std=c["target_std"], noise_std=c["noise_std"],
+                         draft_T=c["draft_T"], ids=c["ids"], device=device, chunk_rows=chunk_rows)
+
+
+def make_workload(*, name: str, B: int, gamma, V: int, dtype: str, T: float, seed: int,
+                  target_std: float = 3.0, noise_std: float | None = 1.0,
+                  draft_T: float | None = None, ids: str = "sample", device="cpu",
+                  chunk_rows: int = 512) -> Workload:
+    """Generic generator.  ``gamma`` is an int or an inclusive range (lo, hi)
+    drawn per request; ``ids`` is "sample" (x ~ q) or "argmax0.75" (greedy
+    drafts that match the target argmax with probability 0.75)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    if isinstance(gamma, tuple):
+        gam = torch.randint(gamma[0], gamma[1] + 1, (B,), generator=g, device=dev)
+    else:
+        gam = torch.full((B,), int(gamma), dtype=torch.int64, device=dev)
+    cu = torch.zeros(B + 1, dtype=torch.int64, device=dev)
+    cu[1:] = torch.cumsum(gam, 0)
+    n_d = int(cu[-1])
+    n_t = n_d + B
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    logits = torch.empty(n_t, V, dtype=tdt, device=dev)
+    for r0 in range(0, n_t, chunk_rows):
+        r1 = min(n_t, r0 + chunk_rows)
+        blk = torch.randn(r1 - r0, V, generator=g, device=dev) * target_std
+        logits[r0:r1] = blk.to(tdt)
+
+    # Target row of draft position d: d + (request index of d).
+    req_of_draft = torch.repeat_interleave(torch.arange(B, device=dev), gam, output_size=n_d)
+    tgt_row_of_draft = torch.arange(n_d, device=dev) + req_of_draft
+
+    draft_probs = None
+    draft_ids = torch.empty(n_d, dtype=torch.int32, device=dev)
+    if ids == "sample":
+        draft_probs = torch.empty(n_d, V, dtype=torch.float32, device=dev)
+        dT = 1.0 if draft_T is None else float(draft_T)
+        for d0 in range(0, n_d, chunk_rows):
+            d1 = min(n_d, d0 + chunk_rows)
+            base = logits[tgt_row_of_draft[d0:d1]].float()
+            noisy = base + torch.randn(d1 - d0, V, generator=g, device=dev) * noise_std
+            q = torch.softmax(noisy / dT, dim=-1)
+            draft_probs[d0:d1] = q
+            draft_ids[d0:d1] = torch.multinomial(q, 1, generator=g).squeeze(1).to(torch.int32)
+    elif ids == "argmax0.75":
+        for d0 in range(0, n_d, chunk_rows):
+            d1 = min(n_d, d0 + chunk_rows)
+            rows = logits[tgt_row_of_draft[d0:d1]].float()
+            am = torch.argmax(rows, dim=-1)      # first maximal index
+            hit = torch.rand(d1 - d0, generator=g, device=dev) < 0.75
+            rnd = torch.randint(0, V, (d1 - d0,), generator=g, device=dev)
+            draft_ids[d0:d1] = torch.where(hit, am, rnd).to(torch.int32)
+    else:
+        raise ValueError(ids)
+    return Workload(name=name, B=B, V=V, dtype=dtype, T=float(T), seed=seed,
+                    target_logits=logits, draft_probs=draft_probs, draft_ids=draft_ids,
+                    cu=cu.to(torch.int32), meta=dict(gamma=gamma, target_std=target_std,
+                                                     noise_std=noise_std, draft_T=draft_T, ids=ids))
+
+
+def to_numpy_logits(t: torch.Tensor):
+    """Target logits as numpy: float32, or the uint16 bit patterns of bf16."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()
+
+
+def from_rows(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
+              draft_ids: torch.Tensor, gammas, T: float, seed: int, name: str = "custom") -> Workload:
+    """Wraps hand-built tensors in a Workload (edge-case tests)."""
+    gam = torch.as_tensor(list(gammas), dtype=torch.int64)
+    cu = torch.zeros(len(gam) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(gam, 0)
+    dtype = "bf16" if target_logits.dtype == torch.bfloat16 else "f32"
+    return Workload(name=name, B=len(gam), V=target_logits.shape[-1], dtype=dtype, T=float(T),
+                    seed=seed, target_logits=target_logits, draft_probs=draft_probs,
+                    draft_ids=draft_ids.to(torch.int32), cu=cu.to(torch.int32))
