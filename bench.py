@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 speculative-sampling verifier.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one verify call over the whole synthetic batch (row kernel, first-
+rejection scan, deferred-race kernel).  Default workload: the large batch
+(B=1024 requests, gamma=7 drafts, V=256000, bf16 target logits, f32 draft
+probabilities, T=1), whose 11.5 GB of inputs dwarf the 129 MB L2, so no L2
+flush is needed between steps.  Prints one JSON line (rank 0).
+
+--impl reference times the CPU oracle (the plain double-precision C
+implementation the tests compare against) on the host cores, on a bounded
+sample of the same workload.
+
+Multi-GPU (torchrun, one rank per GPU): requests are independent, so every rank
+verifies its own full batch (weak scaling, no collective on the data path); the
+barrier and the max over ranks are for timing only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/s"
+UNIT = "positions/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["speculative_decoding_rejection_decode_gb300/csrc/kernels.cuh",
+                  "speculative_decoding_rejection_decode_gb300/csrc/device_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_row_kernel_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=4, help="standard workload 0..4")
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller case)")
+    ap.add_argument("--vocab", type=int, default=None, help="override V")
+    ap.add_argument("--path", choices=["auto", "fused", "sweep", "two_pass"], default="auto")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (timing only)
+# ----------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"specdec_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, power, reasons = [], [], [], set()
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per launch of the row kernel from the committed ncu summary,
+    when it was taken on the current kernel source and this workload."""
+    try:
+        vals = {}
+        for line in open(TRAFFIC_FILE):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("source_sha256_16") != kernel_source_hash():
+            return None
+        if vals.get("workload_key") != workload_key:
+            return None
+        return float(vals["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample_rate(w, seconds: float, start_request: int = 0):
+    """Runs the oracle request by request for about `seconds` of wall time;
+    returns (positions/s, requests done, positions done, elapsed)."""
+    import oracle
+    from speculative_decoding_rejection_decode_gb300.inputs import to_numpy_logits
+    cu = w.cu.cpu().numpy().astype("int64")
+    done_req = done_pos = 0
+    elapsed = 0.0
+    b = start_request
+    while (elapsed < seconds or done_req < 2) and done_req < w.B:
+        b = b % w.B
+        d0, d1 = cu[b], cu[b + 1]
+        tgt = to_numpy_logits(w.target_logits[d0 + b:d1 + b + 1])
+        q = None if w.draft_probs is None else w.draft_probs[d0:d1].cpu().numpy()
+        ids = w.draft_ids[d0:d1].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.verify_request(int(b), tgt, q, ids, w.T, w.seed)
+        elapsed += time.perf_counter() - t0
+        done_req += 1
+        done_pos += int(d1 - d0)
+        b += 1
+    return done_pos / elapsed, done_req, done_pos, elapsed
+
+
+def workload_desc(w, args, flush: bool, in_bytes: int) -> dict:
+    gam = w.meta.get("gamma")
+    return {
+        "workload": f"{w.name} (standard workload {args.config})",
+        "B": w.B, "gamma": list(gam) if isinstance(gam, tuple) else gam, "V": w.V,
+        "target_dtype": w.dtype, "draft_dtype": None if w.draft_probs is None else "f32",
+        "T": w.T, "n_draft_positions": w.n_draft, "n_target_rows": w.n_target,
+        "input_bytes": in_bytes,
+        "l2": ("flushed between steps (256 MB write)" if flush else
+               f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush"),
+    }
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    import torch
+    from speculative_decoding_rejection_decode_gb300.inputs import make_config
+
+    if args.impl == "reference":
+        run_reference(args, dist)
+        dist.close()
+        return
+
+    from speculative_decoding_rejection_decode_gb300.build import build
+    build()
+    import speculative_decoding_rejection_decode_gb300 as sd
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w = make_config(args.config, device=dev, B=args.batch, V=args.vocab)
+    esize = 2 if w.dtype == "bf16" else 4
+    tgt_bytes = w.n_target * w.V * esize
+    drf_bytes = 0 if w.draft_probs is None else w.n_draft * w.V * 4
+    in_bytes = tgt_bytes + drf_bytes
+    flush = in_bytes < 4 * L2_BYTES
+    alg_bytes_step = w.algorithmic_bytes()       # + one extra target row per request
+    alg_bytes_rows = tgt_bytes + drf_bytes       # what the row kernel must read
+    workload_key = f"config{args.config}-B{w.B}-V{w.V}-{args.path}"
+
+    v = sd.Verifier(dev)
+    v.reserve(w.n_draft, w.B)
+    if args.path != "auto":
+        v.set_path({"fused": sd.SPECDEC_PATH_FUSED, "sweep": sd.SPECDEC_PATH_SWEEP,
+                    "two_pass": sd.SPECDEC_PATH_TWO_PASS}[args.path])
+    out = sd.VerifyOutput(tokens=torch.empty(w.n_target, dtype=torch.int32, device=dev),
+                          num_accepted=torch.empty(w.B, dtype=torch.int32, device=dev),
+                          beta=torch.empty(w.n_draft, dtype=torch.float32, device=dev))
+    offset = dist.rank * w.B
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def step():
+        v(w.target_logits, w.draft_probs, w.draft_ids, w.cu, w.T, w.seed, out=out,
+          request_offset=offset)
+
+    for _ in range(max(3, args.warmup)):
+        if flush:
+            scratch.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    if v.get_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    path, csize = v.last_path()
+    launches_per_step = {sd.SPECDEC_PATH_FUSED: 3, sd.SPECDEC_PATH_TWO_PASS: 4,
+                         sd.SPECDEC_PATH_SWEEP: 3, sd.SPECDEC_PATH_GREEDY: 2}[path]
+    kernel_name = {sd.SPECDEC_PATH_FUSED: "fused_row_kernel", sd.SPECDEC_PATH_SWEEP: "sweep_row_kernel",
+                   sd.SPECDEC_PATH_TWO_PASS: "stats_kernel+verify_kernel",
+                   sd.SPECDEC_PATH_GREEDY: "greedy_partial_kernel"}[path]
+    path_name = {1: "fused", 2: "two_pass", 3: "sweep", 4: "greedy"}[path]
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    stream = torch.cuda.current_stream(dev)
+    for e in ev:               # materialise the CUDA events before handing them over
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.25)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    for k in range(K):
+        if flush:
+            scratch.fill_(1.0)
+        s0, r0, r1, s1 = ev[k]
+        v.set_timing_events(r0, r1)
+        s0.record(stream)
+        step()
+        s1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    dist.barrier()
+    clocks = sampler.stop()
+    v.set_timing_events(None, None)
+    if v.get_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    row_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    region_ms = ev[0][0].elapsed_time(ev[-1][3]) if not flush else sum(step_ms)
+    total_s = dist.max(region_ms / 1e3)
+    ms_per_step = total_s * 1e3 / K
+    value = w.n_draft * dist.world * K / total_s
+    row_avg_ms = statistics.mean(row_ms)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = alg_bytes_rows / (row_avg_ms / 1e3) / 1e9
+    traffic = recorded_traffic(workload_key)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_desc(w, args, flush, in_bytes),
+        "requests_per_s": w.B * dist.world * K / total_s,
+        "achieved_gbps_step": alg_bytes_step / (ms_per_step / 1e3) / 1e9,
+        "algorithmic_bytes_per_step": alg_bytes_step,
+        "frac_step_of_peak": alg_bytes_step / (ms_per_step / 1e3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": kernel_name,
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg_bytes_rows,
+                     "avg_launch_ms": row_avg_ms, "min_launch_ms": min(row_ms),
+                     "share_of_step": row_avg_ms / statistics.mean(step_ms)},
+        "path": path_name, "cluster_size": csize,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        rate, nreq, npos, el = oracle_sample_rate(w, args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {nreq} requests ({npos} draft positions) of the same workload, "
+                      f"one thread, {el:.1f} s of oracle time"}
+    if dist.rank == 0:
+        print(json.dumps(result), flush=True)
+    v.close()
+    dist.close()
+
+
+def measure_e2e(v, w, out, dev, stream, steps, dist, offset):
+    """Same metric through the public API with the step's inputs in pinned host
+    memory: every step copies them to the device, verifies, and reads the
+    tokens, counts and beta back."""
+    import torch
+    host = {}
+    for name in ("target_logits", "draft_probs", "draft_ids", "cu"):
+        t = getattr(w, name)
+        if t is None:
+            continue
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host[name] = h
+    h_out = {k: torch.empty(getattr(out, k).shape, dtype=getattr(out, k).dtype, pin_memory=True)
+             for k in ("tokens", "num_accepted", "beta")}
+    h2d = sum(h.numel() * h.element_size() for h in host.values())
+    d2h = sum(h.numel() * h.element_size() for h in h_out.values())
+
+    def one():
+        for name, h in host.items():
+            getattr(w, name).copy_(h, non_blocking=True)
+        v(w.target_logits, w.draft_probs, w.draft_ids, w.cu, w.T, w.seed, out=out,
+          request_offset=offset)
+        for k, h in h_out.items():
+            h.copy_(getattr(out, k), non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    total_s = dist.max(e0.elapsed_time(e1) / 1e3)
+    return {"value": w.n_draft * dist.world * steps / total_s, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": total_s * 1e3 / steps}
+
+
+def run_reference(args, dist):
+    """CPU oracle arm: rank 0 only; each step is the oracle over a bounded
+    sample of the workload (about 2 s of CPU work)."""
+    if dist.rank != 0:
+        return
+    import torch
+    from speculative_decoding_rejection_decode_gb300.inputs import make_config
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = make_config(args.config, device=dev, B=args.batch, V=args.vocab)
+    per_step_s = 2.0
+    for k in range(args.warmup):
+        oracle_sample_rate(w, 0.0, start_request=k)
+    rates, pos, el = [], 0, 0.0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        r, _, p, e = oracle_sample_rate(w, per_step_s, start_request=k * 7)
+        rates.append(r)
+        pos += p
+        el += e
+        if time.perf_counter() - t0 > 150:     # keep the arm within a few minutes
+            break
+    value = pos / el
+    steps_done = len(rates)
+    esize = 2 if w.dtype == "bf16" else 4
+    in_bytes = w.n_target * w.V * esize + (0 if w.draft_probs is None else w.n_draft * w.V * 4)
+    res = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": dist.world, "steps": steps_done, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / max(steps_done, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(w, args, False, in_bytes),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{pos} draft positions over {steps_done} steps of ~{per_step_s:.0f} s "
+                                   "(consecutive requests of the same workload), one thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * specdec.h — C ABI of the GB300 speculative-sampling verifier (libspecdec.so).
+ *
+ * The library runs the verify step of speculative decoding (Leviathan et al.,
+ * "Fast Inference from Transformers via Speculative Decoding", Algorithm 1, as
+ * restated on the bloss0m reading notes "Speculative Decoding：用小模型打草稿、
+ * 大模型一次驗…", sections "Algorithm 1" and "Speculative sampling (Section
+ * 2.3)", and on the vllbc notes "Speculative Decoding：draft 先猜，target 一次
+ * 验证", Algorithm 1 steps 3-4) for a whole batch of requests in one call, on
+ * one GPU, asynchronously on the caller's stream.  Per request b with gamma_b
+ * drafts it
+ *   1. forms p_i = softmax(target_logits_i / T) for i = 0..gamma_b;
+ *   2. tests draft i with r_i < min(1, p_i(x_i) / q_i(x_i)) (strict, as in the
+ *      pseudo-code of the timinsight guide "Speculative Decoding 實作指南", Step 2)
+ *      and stops at the first rejection: n_b = accepted drafts;
+ *   3. draws one more token t: from norm(max(0, p_n - q_n)) when n_b < gamma_b
+ *      (correction), else from p_gamma (bonus);
+ *   4. reports beta_i = sum_v min(p_i(v), q_i(v)) for every draft position
+ *      (Theorem 3.5 / Corollary 3.6 on the same pages).
+ * At T == 0 it runs the greedy reading of the vllbc page's Section 2.2 note
+ * (argmax folds into the adjusted p, q): accept iff x_i equals the target argmax
+ * (lowest index on ties), t = argmax of row n_b, beta_i = [x_i == argmax].
+ *
+ * Randomness is counter based, so a call is a pure function of its inputs and
+ * `seed` (SplitMix64 of Steele, Lea and Flood, OOPSLA 2014):
+ *     sm(z)  = SplitMix64 finaliser applied to z + 0x9E3779B97F4A7C15
+ *     key    = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream))
+ *     U      = ((sm(key ^ v) >> 41) + 0.5) * 2^-23          (exact in float32)
+ * r_i = U(seed, b, i, stream 0, v 0); the extra token is the exponential race
+ * t = argmax_v w(v) / E_v with E_v = -ln U(seed, b, n_b, stream 1, v), an exact
+ * sampler of norm(w) that needs no normaliser and no prefix scan.
+ *
+ * Batch layout (the flattened ragged batch that the vllbc page describes for
+ * vLLM's rejection sampler, `cu_num_draft_tokens`):
+ *   cu[0] = 0, cu[b+1] = cu[b] + gamma_b, N_d = cu[B], N_t = N_d + B.
+ *   draft row / id of (b, i), i < gamma_b : cu[b] + i
+ *   target row of (b, i),     i <= gamma_b: cu[b] + b + i   (i = gamma_b: bonus row)
+ *   output token slot of (b, i)           : cu[b] + b + i
+ * All matrices are row-major and contiguous: target_logits [N_t, V],
+ * draft_probs [N_d, V].
+ *
+ * Ownership: the caller owns every input and output buffer (device memory).  The
+ * handle owns a device workspace (per-row softmax statistics and status words,
+ * about 24 bytes per target row plus 8 bytes per request) and one stream-ordered
+ * error word.  A handle serves one stream at a time; calls on it are
+ * asynchronous and never synchronise, except the first call that needs a larger
+ * workspace than specdec_reserve() provided (it reads cu[B] back to size it).
+ *
+ * Errors: host-checked problems return a negative status before anything is
+ * launched.  Problems only the device can see (a draft id outside [0, V), a
+ * cu array that does not start at 0 or decreases, more rows than the reserved
+ * workspace) set bits of the handle's sticky device error word, never trap, and
+ * leave the affected outputs defined: a bad draft id is treated as a rejected
+ * draft with p(x) = q(x) = 0; a bad cu or capacity overflow writes nothing.
+ */
+#ifndef SPECDEC_H
+#define SPECDEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct specdec_ctx* specdec_handle_t;
+
+/* dtype of target_logits (draft_probs are always float32) */
+#define SPECDEC_F32 0
+#define SPECDEC_BF16 1
+
+/* status codes */
+#define SPECDEC_OK 0
+#define SPECDEC_ERR_INVALID_ARG (-1)
+#define SPECDEC_ERR_UNSUPPORTED_DTYPE (-2)
+#define SPECDEC_ERR_CUDA (-3)
+#define SPECDEC_ERR_OOM (-4)
+#define SPECDEC_ERR_BAD_DRAFT_ID (-5)
+#define SPECDEC_ERR_CAPACITY (-6)
+#define SPECDEC_ERR_TIMEOUT (-7)
+
+/* bits of the device error word */
+#define SPECDEC_DEVERR_BAD_DRAFT_ID 1u
+#define SPECDEC_DEVERR_BAD_CU 2u
+#define SPECDEC_DEVERR_CAPACITY 4u
+#define SPECDEC_DEVERR_TIMEOUT 8u
+
+/* execution paths (specdec_set_path); AUTO picks per call */
+#define SPECDEC_PATH_AUTO 0
+#define SPECDEC_PATH_FUSED 1    /* cluster-staged single HBM pass (T > 0)            */
+#define SPECDEC_PATH_TWO_PASS 2 /* statistics kernel, then verify kernel (T > 0)     */
+#define SPECDEC_PATH_SWEEP 3    /* one CTA per row pair, second sweep from L2 (T > 0) */
+#define SPECDEC_PATH_GREEDY 4   /* reported by specdec_last_path for T == 0          */
+
+/* Creates a handle bound to CUDA device `device`.  *out receives the handle.
+ * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (null out, bad device) or
+ * SPECDEC_ERR_CUDA. */
+int specdec_create(specdec_handle_t* out, int device);
+
+/* Pre-sizes the workspace for calls with cu[B] <= max_draft_positions and
+ * B <= max_batch, so that later calls within those bounds allocate nothing and
+ * never read cu back to the host.  Optional.  Returns SPECDEC_OK,
+ * SPECDEC_ERR_INVALID_ARG or SPECDEC_ERR_OOM. */
+int specdec_reserve(specdec_handle_t h, int64_t max_draft_positions, int max_batch);
+
+/* One verify step for B requests (see the top of this file for the layout).
+ *   target_logits      device [N_t, V] of `dtype`; 16-byte aligned rows take the
+ *                      single-pass path, other strides a two-pass path
+ *   dtype              SPECDEC_F32 or SPECDEC_BF16
+ *   draft_probs        device [N_d, V] float32 rows of q (taken as given, not
+ *                      renormalised); ignored and may be NULL when T == 0, a
+ *                      valid pointer otherwise (even when N_d == 0)
+ *   draft_ids          device [N_d] int32 (a valid pointer even when N_d == 0)
+ *   cu_num_draft_tokens device [B+1] int32, cu[0] = 0, non-decreasing
+ *   B, V               requests (>= 1) and vocabulary size (1 .. 2^30)
+ *   T                  temperature: > 0 samples, == 0 greedy; NaN, inf or < 0 is
+ *                      SPECDEC_ERR_INVALID_ARG
+ *   seed               generator seed
+ *   out_tokens         device [N_t] int32: slots cu[b]+b .. cu[b]+b+n_b-1 get the
+ *                      accepted drafts, slot cu[b]+b+n_b the correction / bonus
+ *                      token, later slots of the request -1
+ *   out_num_accepted   device [B] int32: n_b in [0, gamma_b]
+ *   out_beta           device [N_d] float32 beta_i for every draft position, or NULL
+ *   stream             cudaStream_t (NULL = legacy default stream)
+ * Returns SPECDEC_OK once the kernels are queued, a negative status otherwise. */
+int specdec_rejection_sample(specdec_handle_t h, const void* target_logits, int dtype,
+                             const float* draft_probs, const int32_t* draft_ids,
+                             const int32_t* cu_num_draft_tokens, int B, int V, float T,
+                             uint64_t seed, int32_t* out_tokens, int32_t* out_num_accepted,
+                             float* out_beta, void* stream);
+
+/* As specdec_rejection_sample, with three more optional per-draft-position
+ * outputs (device [N_d], each may be NULL):
+ *   out_target_prob   p_i(x_i) (0 for an out-of-range id; [x_i == argmax] at T == 0)
+ *   out_draft_prob    q_i(x_i) (0 for an out-of-range id; 1 at T == 0)
+ *   out_accept        int32 result of the accept test at every position, also
+ *                     after the first rejection, where it no longer matters
+ * and `request_offset`: request b of this call uses generator index
+ * request_offset + b, so a batch split into shards (one call per GPU, each
+ * with the index of its first request) draws exactly what one call over the
+ * whole batch draws.  specdec_rejection_sample uses 0. */
+int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, int dtype,
+                                const float* draft_probs, const int32_t* draft_ids,
+                                const int32_t* cu_num_draft_tokens, int B, int V, float T,
+                                uint64_t seed, uint64_t request_offset, int32_t* out_tokens,
+                                int32_t* out_num_accepted, float* out_beta,
+                                float* out_target_prob, float* out_draft_prob,
+                                int32_t* out_accept, void* stream);
+
+/* Reads the handle's sticky device error word (SPECDEC_DEVERR_* bits) into
+ * *device_error and clears it.  Queues the read on `stream` and waits for it, so
+ * it reports every call queued on that stream before it.  Returns SPECDEC_OK or
+ * SPECDEC_ERR_CUDA. */
+int specdec_get_error(specdec_handle_t h, int* device_error, void* stream);
+
+/* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP or
+ * _AUTO, the default).  A forced FUSED path falls back to SWEEP where its layout
+ * rules (16-byte aligned rows, a vocabulary that fits a cluster) do not hold. */
+int specdec_set_path(specdec_handle_t h, int path);
+
+/* Profiling hook: when set, every later call records `before_rows`
+ * (cudaEvent_t) on its stream just before the row kernel(s) and `after_rows`
+ * just after them, so a caller can time the dominant kernel on its own stream.
+ * Pass NULL, NULL to stop.  The events stay owned by the caller. */
+int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after_rows);
+
+/* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP
+ * or _GREEDY), and the cluster size of the fused path (0 otherwise). */
+int specdec_last_path(specdec_handle_t h, int* path, int* cluster_size);
+
+/* Writes out[j] = U(seed, b, pos, stream_id, v0 + j) for j < n into device
+ * memory `out` (float32, exact), from the same device code the verifier uses.
+ * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG or SPECDEC_ERR_CUDA. */
+int specdec_uniform(uint64_t seed, uint64_t b, uint64_t pos, uint32_t stream_id, uint64_t v0,
+                    int64_t n, float* out, void* stream);
+
+/* Diagnostic: writes out[j] = E(k0 + j) = -ln U for the 23-bit uniform
+ * U = (k + 1/2) 2^-23, k = k0 + j < 2^23, computed by the same device code the
+ * race uses (so tests can bound its error against double precision). */
+int specdec_neg_log_uniform(uint32_t k0, int64_t n, float* out, void* stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* specdec_status_string(int status);
+
+/* Frees the handle and its workspace (waits for work queued on it). */
+int specdec_destroy(specdec_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_H */

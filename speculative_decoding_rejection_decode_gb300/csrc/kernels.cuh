@@ -1,0 +1,1008 @@
+// Verifier kernels.
+//
+//   fused_row_kernel   one HBM pass per (target row, draft row) pair.  A cluster
+//                      of C CTAs holds the target row in shared memory (bulk
+//                      copies), reduces (max, sum) across the cluster through
+//                      distributed shared memory, then streams the draft row once
+//                      for beta = sum min(p, q), the accept test and, when this
+//                      row is the request's first rejection (or its bonus row after
+//                      all drafts were accepted), the exponential race that draws
+//                      the extra token.
+//   stats_kernel +     the two-pass form for layouts the bulk copies cannot take
+//   verify_kernel      (unaligned rows) or vocabularies too large for a cluster.
+//   finalize_kernel    per-request first-rejection scan over cu_num_draft_tokens.
+//   race_kernel        the race for requests whose extra token the row kernel could
+//                      not draw (its row ran before the earlier rows of the request
+//                      finished): re-reads that single row.
+//   greedy_*           T = 0: argmax partials per row slice, then the scan.
+//
+// Method: Algorithm 1 and Section 2.3 of Leviathan et al. as restated on the
+// bloss0m and vllbc reading-notes pages; accept test r < min(1, p/q) as in the
+// timinsight guide's Step 2 pseudo-code; beta from Theorem 3.5.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace specdec {
+
+// ---------------------------------------------------------------------------
+// Shared parameter block.
+// ---------------------------------------------------------------------------
+struct Params {
+  const void* logits;      // [N_t, V] float or bf16
+  const float* q;          // [N_d, V] or null (greedy)
+  const int32_t* ids;      // [N_d]
+  const int32_t* cu;       // [B+1]
+  int B;
+  int V;
+  float c;                 // log2(e) / T
+  uint64_t seed;
+  uint64_t req_offset;     // generator request index = req_offset + b
+  uint64_t epoch;          // call counter (status words of this call carry it)
+  int32_t* out_tokens;     // [N_t]
+  int32_t* out_nacc;       // [B]
+  float* out_beta;         // [N_d] or null
+  float* out_px;           // [N_d] or null
+  float* out_qx;           // [N_d] or null
+  int32_t* out_acc;        // [N_d] or null
+  // workspace
+  float2* row_stats;       // [cap_rows] (max, sum) of each target row
+  uint64_t* status;        // [cap_rows]
+  uint64_t* gkeys;         // [cap_rows * gparts] greedy partial argmax keys
+  int32_t* ws_nacc;        // [cap_B] n_b for the race kernel
+  int32_t* defer_list;     // [cap_B]
+  int32_t* defer_count;    // [1]
+  unsigned long long* sched;  // [1] next work slot of the sweep kernel (reset by finalize)
+  uint32_t* err;           // [1] sticky device error word
+  int64_t cap_rows;
+  int cap_b;
+  int gparts;              // greedy: slices per row
+  int gpart_len;           // greedy: elements per slice (multiple of 8)
+  // fused kernel geometry
+  int slice_len;           // elements per cluster rank (multiple of 8)
+  int tbuf_bytes;          // bytes of the target slice buffer (rank 0, 128-aligned)
+  int nq;                  // draft ring stages
+  int vec_ok;              // rows are 16-byte aligned: vector loads allowed
+};
+
+constexpr int kChunk = 4096;          // elements per bulk copy / pipeline step
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kFusedThreads = kConsumers + 32;  // + one producer warp
+constexpr int kMaxCluster = 16;
+constexpr int kMaxChunks = 64;
+
+__device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
+
+// ---------------------------------------------------------------------------
+// Fused single-pass row kernel (T > 0).
+// ---------------------------------------------------------------------------
+struct alignas(16) FusedShared {
+  uint64_t tfull[kMaxChunks];
+  uint64_t tempty[kMaxChunks];
+  uint64_t qfull[16];
+  uint64_t qempty[16];
+  uint64_t x1full[2];
+  uint64_t x2full[2];
+  float4 xch1[2][kMaxCluster];   // (max, sum, prefix state, -) from every rank
+  float4 xch2[2][kMaxCluster];   // (beta, race w, race e, race index) at rank 0
+  float4 red[2][kConsumerWarps];
+  int gmax;
+  int bad;
+  volatile int abort_flag;
+};
+
+template <typename TT>
+__global__ void __launch_bounds__(kFusedThreads, 1) fused_row_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  constexpr int kEl = 16 / sizeof(TT);  // elements per 16-byte target vector
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t C = cluster_nctarank();
+  const uint32_t cid = cluster_id_x();
+  const uint32_t ncl = ncluster_x();
+
+  TT* tbuf = reinterpret_cast<TT*>(smem_raw);
+  float* qring = reinterpret_cast<float*>(smem_raw + P.tbuf_bytes);
+  FusedShared& S = *reinterpret_cast<FusedShared*>(smem_raw + P.tbuf_bytes +
+                                                   (size_t)P.nq * kChunk * sizeof(float));
+
+  const int V = P.V, B = P.B;
+  const int s0 = min((int)rank * P.slice_len, V);
+  const int s1 = min(s0 + P.slice_len, V);
+  const int slen = s1 - s0;
+  const int nch = (slen + kChunk - 1) / kChunk;
+
+  // ---- prologue: barriers, scan of cu (largest gamma, validity) ----------
+  if (tid == 0) {
+    for (int j = 0; j < nch; ++j) {
+      mbar_init(smem_addr(&S.tfull[j]), 1);
+      mbar_init(smem_addr(&S.tempty[j]), kConsumerWarps);
+    }
+    for (int s = 0; s < P.nq; ++s) {
+      mbar_init(smem_addr(&S.qfull[s]), 1);
+      mbar_init(smem_addr(&S.qempty[s]), kConsumerWarps);
+    }
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(smem_addr(&S.x1full[p]), C);
+      mbar_init(smem_addr(&S.x2full[p]), C);
+    }
+    S.gmax = 0;
+    S.bad = 0;
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  {
+    int gm = 0, bad = 0;
+    for (int b = tid; b < B; b += blockDim.x) {
+      int g = __ldg(P.cu + b + 1) - __ldg(P.cu + b);
+      gm = max(gm, g);
+      bad |= (g < 0);
+    }
+    if (gm) atomicMax(&S.gmax, gm);
+    if (bad) atomicOr(&S.bad, 1);
+  }
+  cluster_sync_all();  // barrier inits visible cluster-wide; gmax / bad final
+  if (cid == 0 && rank == 0 && tid == 0) {
+    if (S.bad || __ldg(P.cu) != 0) set_err(P.err, SPECDEC_DEVERR_BAD_CU);
+    if (P.defer_count) *P.defer_count = 0;
+  }
+  const int gmax = S.gmax;
+  const int64_t total_slots = (int64_t)B * (gmax + 1);
+
+  if (warp == kConsumerWarps) {
+    // ===================== producer warp ====================================
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t uc = 0, qc = 0;
+      uint32_t t_issued[kMaxChunks];
+      uint32_t q_issued[16];
+      for (int j = 0; j < nch; ++j) t_issued[j] = 0;
+      for (int s = 0; s < P.nq; ++s) q_issued[s] = 0;
+      for (int64_t u = cid; u < total_slots && !S.abort_flag; u += ncl) {
+        const int i = (int)(u / B), b = (int)(u % B);
+        const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+        if (i > g) continue;
+        const int64_t t = (int64_t)c0 + b + i;
+        if (t >= P.cap_rows) continue;
+        const bool has_q = i < g;
+        const TT* trow = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V + s0;
+        for (int j = 0; j < nch; ++j) {
+          if (!mbar_wait(smem_addr(&S.tempty[j]), (uc & 1) ^ 1)) {
+            S.abort_flag = 1;
+            break;
+          }
+          const int n = min(kChunk, slen - j * kChunk);
+          mbar_arrive_expect_tx(smem_addr(&S.tfull[j]), n * sizeof(TT));
+          bulk_load(smem_addr(tbuf + j * kChunk), trow + j * kChunk, n * sizeof(TT),
+                    smem_addr(&S.tfull[j]), pol);
+          ++t_issued[j];
+        }
+        if (has_q && !S.abort_flag) {
+          const float* qrow = P.q + ((int64_t)c0 + i) * (int64_t)V + s0;
+          for (int j = 0; j < nch; ++j, ++qc) {
+            const int s = qc % P.nq;
+            if (!mbar_wait(smem_addr(&S.qempty[s]), ((qc / P.nq) & 1) ^ 1)) {
+              S.abort_flag = 1;
+              break;
+            }
+            const int n = min(kChunk, slen - j * kChunk);
+            mbar_arrive_expect_tx(smem_addr(&S.qfull[s]), n * 4);
+            bulk_load(smem_addr(qring + (size_t)s * kChunk), qrow + j * kChunk, n * 4,
+                      smem_addr(&S.qfull[s]), pol);
+            ++q_issued[s];
+          }
+        }
+        ++uc;
+      }
+      if (S.abort_flag) {
+        // Let every copy this CTA issued land before the CTA can exit.
+        set_err(P.err, SPECDEC_DEVERR_TIMEOUT);
+        for (int j = 0; j < nch; ++j)
+          if (t_issued[j]) mbar_wait(smem_addr(&S.tfull[j]), (t_issued[j] - 1) & 1);
+        for (int s = 0; s < P.nq; ++s)
+          if (q_issued[s]) mbar_wait(smem_addr(&S.qfull[s]), (q_issued[s] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== consumer warps ===================================
+    uint32_t uc = 0, qc = 0;
+    for (int64_t u = cid; u < total_slots; u += ncl) {
+      const int i = (int)(u / B), b = (int)(u % B);
+      const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+      if (i > g) continue;
+      const int64_t t = (int64_t)c0 + b + i;
+      if (t >= P.cap_rows) {
+        if (tid == 0 && rank == 0) set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+        continue;
+      }
+      const int64_t d = (int64_t)c0 + i;
+      const bool has_q = i < g;
+      const int par = uc & 1;
+      bool ok = true;
+
+      // ---- pass 1: (max, sum) of this rank's slice ---------------------------
+      float m = -INFINITY, s = 0.0f;
+      for (int j = 0; j < nch; ++j) {
+        ok &= S.abort_flag ? false : mbar_wait(smem_addr(&S.tfull[j]), uc & 1);
+        const int n = min(kChunk, slen - j * kChunk);
+        const TT* ch = tbuf + j * kChunk;
+        for (int e = tid * kEl; e < n; e += kConsumers * kEl) {
+          float x[kEl];
+          if constexpr (sizeof(TT) == 2) {
+            uint4 w = *reinterpret_cast<const uint4*>(ch + e);
+            x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+            x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+          } else {
+            float4 w = *reinterpret_cast<const float4*>(ch + e);
+            x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+          }
+          float vm = x[0];
+#pragma unroll
+          for (int k = 1; k < kEl; ++k) vm = fmaxf(vm, x[k]);
+          if (vm > m) {
+            s *= ex2((m - vm) * P.c);
+            m = vm;
+          }
+          if (m != -INFINITY) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kEl; ++k) acc += ex2((x[k] - m) * P.c);
+            s += acc;
+          }
+        }
+      }
+      warp_softmax(m, s, P.c);
+      if (lane == 0) S.red[par][warp] = make_float4(m, s, 0.f, 0.f);
+      named_bar_sync(1, kConsumers);
+      m = -INFINITY;
+      s = 0.0f;
+      for (int w = 0; w < kConsumerWarps; ++w) softmax_merge(m, s, S.red[par][w].x, S.red[par][w].y, P.c);
+
+      // ---- exchange 1: every rank gets every rank's (max, sum) --------------
+      if (tid == 0) {
+        int prefix = kPrefixAllAccepted;
+        if (rank == 0 && i > 0) prefix = read_prefix(P.status, t - i, i, P.epoch);
+        const uint32_t slot = smem_addr(&S.xch1[par][rank]);
+        for (uint32_t r = 0; r < C; ++r) {
+          st_cluster_v4(mapa(slot, r), m, s, __int_as_float(prefix), 0.f);
+          mbar_arrive_cluster(mapa(smem_addr(&S.x1full[par]), r));
+        }
+      }
+      ok &= S.abort_flag ? false : mbar_wait_cluster(smem_addr(&S.x1full[par]), (uc >> 1) & 1);
+      float M = -INFINITY, Ssum = 0.0f;
+      for (uint32_t r = 0; r < C; ++r) softmax_merge(M, Ssum, S.xch1[par][r].x, S.xch1[par][r].y, P.c);
+      const int prefix = __float_as_int(S.xch1[par][0].z);
+      const float invS = 1.0f / Ssum;
+
+      // ---- accept test (identical in every thread of every rank) -------------
+      int x = -1;
+      float px = 0.0f, qx = 0.0f;
+      bool acc = false, valid = true;
+      if (has_q) {
+        x = __ldg(P.ids + d);
+        valid = (x >= 0 && x < V);
+        if (valid) {
+          const float lx = load_logit(reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V + x);
+          px = ex2((lx - M) * P.c) * invS;
+          qx = __ldg(P.q + d * (int64_t)V + x);
+        }
+        const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
+        acc = accept_test(r, px, qx);
+      }
+      const bool race = (prefix == kPrefixAllAccepted) && (!has_q || !acc);
+      const bool resid = has_q && !acc;
+      const uint64_t rkey = stream_key(P.seed, P.req_offset + b, i, 1);
+
+      // ---- pass 2: beta and the race over the slice -------------------------
+      float beta = 0.0f;
+      Race best = race_none();
+      for (int j = 0; j < nch; ++j) {
+        const int n = min(kChunk, slen - j * kChunk);
+        int st = 0;
+        if (has_q) {
+          st = qc % P.nq;
+          ok &= S.abort_flag ? false : mbar_wait(smem_addr(&S.qfull[st]), (qc / P.nq) & 1);
+        }
+        if (has_q || race) {
+          const TT* ch = tbuf + j * kChunk;
+          const float* qch = qring + (size_t)st * kChunk;
+          for (int e = tid * 4; e < n; e += kConsumers * 4) {
+            float l[4];
+            if constexpr (sizeof(TT) == 2) {
+              uint2 w = *reinterpret_cast<const uint2*>(ch + e);
+              l[0] = bf16_lo(w.x); l[1] = bf16_hi(w.x); l[2] = bf16_lo(w.y); l[3] = bf16_hi(w.y);
+            } else {
+              float4 w = *reinterpret_cast<const float4*>(ch + e);
+              l[0] = w.x; l[1] = w.y; l[2] = w.z; l[3] = w.w;
+            }
+            float p[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) p[k] = ex2((l[k] - M) * P.c) * invS;
+            if (has_q) {
+              float4 w = *reinterpret_cast<const float4*>(qch + e);
+              qv[0] = w.x; qv[1] = w.y; qv[2] = w.z; qv[3] = w.w;
+              beta += (fminf(p[0], qv[0]) + fminf(p[1], qv[1])) +
+                      (fminf(p[2], qv[2]) + fminf(p[3], qv[3]));
+            }
+            if (race) {
+              const int v0 = s0 + j * kChunk + e;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                race_offer(best, resid ? fmaxf(p[k] - qv[k], 0.0f) : p[k], rkey, (uint32_t)(v0 + k));
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_addr(&S.tempty[j]));
+          if (has_q) mbar_arrive(smem_addr(&S.qempty[st]));
+        }
+        if (has_q) ++qc;
+      }
+      beta = warp_sum(beta);
+      warp_race(best);
+      if (lane == 0) S.red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
+      named_bar_sync(1, kConsumers);
+
+      // ---- exchange 2: partial beta / race to rank 0, which writes outputs ---
+      if (tid == 0) {
+        float bsum = 0.0f;
+        Race cb = race_none();
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float4 r4 = S.red[par ^ 1][w];
+          bsum += r4.x;
+          race_merge(cb, r4.y, r4.z, __float_as_int(r4.w));
+        }
+        st_cluster_v4(mapa(smem_addr(&S.xch2[par][rank]), 0), bsum, cb.w, cb.e, __int_as_float(cb.idx));
+        mbar_arrive_cluster(mapa(smem_addr(&S.x2full[par]), 0));
+        if (rank == 0) {
+          ok &= S.abort_flag ? false : mbar_wait_cluster(smem_addr(&S.x2full[par]), (uc >> 1) & 1);
+          float btot = 0.0f;
+          Race tb = race_none();
+          for (uint32_t r = 0; r < C; ++r) {
+            const float4 r4 = S.xch2[par][r];
+            btot += r4.x;
+            race_merge(tb, r4.y, r4.z, __float_as_int(r4.w));
+          }
+          if (ok) {
+            P.row_stats[t] = make_float2(M, Ssum);
+            uint32_t flags = kStDone;
+            if (has_q) {
+              if (!valid) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+              if (acc) flags |= kStAccepted;
+              if (P.out_beta) P.out_beta[d] = btot;
+              if (P.out_px) P.out_px[d] = px;
+              if (P.out_qx) P.out_qx[d] = qx;
+              if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+            }
+            if (race && tb.w > 0.0f) {
+              P.out_tokens[t] = tb.idx;
+              flags |= kStRaceDone;
+            }
+            st_relaxed_u64(P.status + t, make_status(P.epoch, flags));
+          }
+        }
+      }
+      ++uc;
+      if (named_bar_or(1, kConsumers, !ok || S.abort_flag)) {
+        S.abort_flag = 1;
+        if (tid == 0) set_err(P.err, SPECDEC_DEVERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();  // no rank leaves while a peer may still touch its shared memory
+}
+
+// ---------------------------------------------------------------------------
+// Sweep row kernel (T > 0): one CTA per SM, one (target row, draft row) pair at
+// a time.  Sweep 1 reads the target row from HBM (L2 evict_last) for (max, sum);
+// sweep 2 reads it again, now from L2 (evict_first), together with the draft
+// row (evict_first) for beta, the accept test and the race.  About one target
+// row per SM is live in L2 at a time (~78 MB for V = 256000 bf16).  Work slots
+// are taken in position-major order (every request's position 0, then every
+// position 1, ...) from a global counter, so the earlier rows of a request are
+// usually finished when a later row starts: the row that turns out to be the
+// request's first rejection (or the bonus row after all drafts were accepted)
+// draws the extra token in the same sweep, and a bonus row whose request already
+// rejected a draft is not read at all.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ldg_hint(const void* p, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+template <typename TT>
+__device__ __forceinline__ void unpack16(const uint4& w, float* x) {
+  if constexpr (sizeof(TT) == 2) {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+  } else {
+    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+  }
+}
+
+// Online (max, sum) update with one 16-byte vector of logits.
+template <typename TT>
+__device__ __forceinline__ void softmax_acc16(const uint4& w, float& m, float& s, float c) {
+  constexpr int kEl = 16 / sizeof(TT);
+  float x[kEl];
+  unpack16<TT>(w, x);
+  float vm = x[0];
+#pragma unroll
+  for (int k = 1; k < kEl; ++k) vm = fmaxf(vm, x[k]);
+  if (vm > m) {
+    s *= ex2((m - vm) * c);
+    m = vm;
+  }
+  if (m != -INFINITY) {
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kEl; ++k) a += ex2((x[k] - m) * c);
+    s += a;
+  }
+}
+
+// Sweep-2 work on 4 consecutive vocabulary entries starting at v.
+template <bool kHasQ, bool kRace>
+__device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float M, float c,
+                                         float invS, bool resid, uint64_t rkey, uint32_t v,
+                                         float& beta, Race& best) {
+  const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+  float p[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) p[k] = ex2((l[k] - M) * c) * invS;
+  if constexpr (kHasQ)
+    beta += (fminf(p[0], qv[0]) + fminf(p[1], qv[1])) + (fminf(p[2], qv[2]) + fminf(p[3], qv[3]));
+  if constexpr (kRace) {
+    float e[4];
+    uint32_t kb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) kb[k] = uniform_bits(rkey, v + k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) e[k] = neg_log_uniform(kb[k]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      race_merge(best, (kHasQ && resid) ? fmaxf(p[k] - qv[k], 0.0f) : p[k], e[k], (int32_t)(v + k));
+  }
+}
+
+template <typename TT, int NT, bool kHasQ, bool kRace>
+__device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, bool vec,
+                                       float M, float c, float invS, bool resid, uint64_t rkey,
+                                       uint64_t pol, float& beta, Race& best) {
+  constexpr int kEl = 16 / sizeof(TT);
+  const int tid = threadIdx.x;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (vec) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    const uint4* qv = reinterpret_cast<const uint4*>(qrow);
+    const int nv = V / kEl;
+    int j = tid;
+    for (; j + NT < nv; j += 2 * NT) {
+      uint4 a[2];
+      uint4 b[2][kEl / 4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        a[u] = ldg_hint(rv + j + u * NT, pol);
+        if constexpr (kHasQ) {
+#pragma unroll
+          for (int h = 0; h < kEl / 4; ++h) b[u][h] = ldg_hint(qv + (j + u * NT) * (kEl / 4) + h, pol);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float x[kEl];
+        unpack16<TT>(a[u], x);
+#pragma unroll
+        for (int h = 0; h < kEl / 4; ++h) {
+          float4 q4 = zero4;
+          if constexpr (kHasQ) q4 = *reinterpret_cast<const float4*>(&b[u][h]);
+          sweep2_4<kHasQ, kRace>(x + 4 * h, q4, M, c, invS, resid, rkey,
+                                 (uint32_t)((j + u * NT) * kEl + 4 * h), beta, best);
+        }
+      }
+    }
+    for (; j < nv; j += NT) {
+      float x[kEl];
+      unpack16<TT>(ldg_hint(rv + j, pol), x);
+#pragma unroll
+      for (int h = 0; h < kEl / 4; ++h) {
+        float4 q4 = zero4;
+        if constexpr (kHasQ) {
+          uint4 w = ldg_hint(qv + j * (kEl / 4) + h, pol);
+          q4 = *reinterpret_cast<const float4*>(&w);
+        }
+        sweep2_4<kHasQ, kRace>(x + 4 * h, q4, M, c, invS, resid, rkey, (uint32_t)(j * kEl + 4 * h),
+                               beta, best);
+      }
+    }
+  } else {
+    for (int v = tid; v < V; v += NT) {
+      const float p = ex2((load_logit(row + v) - M) * c) * invS;
+      float qv = 0.0f;
+      if constexpr (kHasQ) {
+        qv = __ldg(qrow + v);
+        beta += fminf(p, qv);
+      }
+      if constexpr (kRace) race_offer(best, (kHasQ && resid) ? fmaxf(p - qv, 0.0f) : p, rkey, (uint32_t)v);
+    }
+  }
+}
+
+template <typename TT, int NT>
+__global__ void __launch_bounds__(NT, 1) sweep_row_kernel(const Params P) {
+  constexpr int NW = NT / 32;
+  constexpr int kEl = 16 / sizeof(TT);
+  __shared__ float4 red[2][NW];
+  __shared__ long long s_slot;
+  __shared__ int s_gmax, s_bad, s_prefix;
+  __shared__ float s_dec[4];  // px, qx, flags
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = P.B, V = P.V;
+  const bool vec = P.vec_ok != 0;
+
+  if (tid == 0) {
+    s_gmax = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  {
+    int gm = 0, bad = 0;
+    for (int b = tid; b < B; b += NT) {
+      const int g = __ldg(P.cu + b + 1) - __ldg(P.cu + b);
+      gm = max(gm, g);
+      bad |= (g < 0);
+    }
+    if (gm) atomicMax(&s_gmax, gm);
+    if (bad) atomicOr(&s_bad, 1);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tid == 0) {
+    if (s_bad || __ldg(P.cu) != 0) set_err(P.err, SPECDEC_DEVERR_BAD_CU);
+    *P.defer_count = 0;
+  }
+  const int64_t total = (int64_t)B * (s_gmax + 1);
+  const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+
+  for (int it = 0;; ++it) {
+    // ---- thread 0 takes the next slot that has a row to verify -------------
+    if (tid == 0) {
+      long long u;
+      int prefix = kPrefixAllAccepted;
+      while (true) {
+        u = (long long)atomicAdd(P.sched, 1ull);
+        if (u >= total) break;
+        const int i = (int)(u / B), b = (int)(u % B);
+        const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+        if (i > g) continue;
+        const int64_t t = (int64_t)c0 + b + i;
+        if (t >= P.cap_rows) {
+          set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+          continue;
+        }
+        prefix = i > 0 ? read_prefix(P.status, t - i, i, P.epoch) : kPrefixAllAccepted;
+        if (i == g && prefix == kPrefixRejected) continue;  // bonus row nobody needs
+        break;
+      }
+      s_slot = u;
+      s_prefix = prefix;
+    }
+    __syncthreads();
+    const long long u = s_slot;
+    const int prefix = s_prefix;
+    if (u >= total) break;
+    const int i = (int)(u / B), b = (int)(u % B);
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t = (int64_t)c0 + b + i, d = (int64_t)c0 + i;
+    const bool has_q = i < g;
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    const float* qrow = has_q ? P.q + d * (int64_t)V : nullptr;
+    const int par = it & 1;
+
+    // thread 0 fetches what the accept test needs while sweep 1 runs
+    int x = -1;
+    float lx = 0.0f, qx = 0.0f;
+    bool valid = true;
+    if (tid == 0 && has_q) {
+      x = __ldg(P.ids + d);
+      valid = (x >= 0 && x < V);
+      if (valid) {
+        lx = load_logit(row + x);
+        qx = __ldg(qrow + x);
+      }
+    }
+
+    // ---- sweep 1: (max, sum) ------------------------------------------------
+    float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+    if (vec) {
+      const uint4* rv = reinterpret_cast<const uint4*>(row);
+      const int nv = V / kEl;
+      int j = tid;
+      for (; j + 3 * NT < nv; j += 4 * NT) {
+        const uint4 a0 = ldg_hint(rv + j, keep), a1 = ldg_hint(rv + j + NT, keep);
+        const uint4 a2 = ldg_hint(rv + j + 2 * NT, keep), a3 = ldg_hint(rv + j + 3 * NT, keep);
+        softmax_acc16<TT>(a0, m0, s0, P.c);
+        softmax_acc16<TT>(a1, m1, s1, P.c);
+        softmax_acc16<TT>(a2, m0, s0, P.c);
+        softmax_acc16<TT>(a3, m1, s1, P.c);
+      }
+      for (; j < nv; j += NT) softmax_acc16<TT>(ldg_hint(rv + j, keep), m0, s0, P.c);
+    } else {
+      for (int v = tid; v < V; v += NT) {
+        const float xv = load_logit(row + v);
+        if (xv > m0) {
+          s0 *= ex2((m0 - xv) * P.c);
+          m0 = xv;
+        }
+        if (m0 != -INFINITY) s0 += ex2((xv - m0) * P.c);
+      }
+    }
+    softmax_merge(m0, s0, m1, s1, P.c);
+    warp_softmax(m0, s0, P.c);
+    if (lane == 0) red[par][warp] = make_float4(m0, s0, 0.f, 0.f);
+    __syncthreads();
+    float M = -INFINITY, S = 0.0f;
+    for (int w = 0; w < NW; ++w) softmax_merge(M, S, red[par][w].x, red[par][w].y, P.c);
+    const float invS = 1.0f / S;
+
+    // ---- accept test (thread 0) and the race decision --------------------
+    if (tid == 0) {
+      float px = 0.0f;
+      bool acc = false;
+      if (has_q) {
+        if (valid) px = ex2((lx - M) * P.c) * invS;
+        const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
+        acc = accept_test(r, px, qx);
+      }
+      const bool race = (prefix == kPrefixAllAccepted) && (!has_q || !acc);
+      s_dec[0] = px;
+      s_dec[1] = qx;
+      s_dec[2] = __int_as_float((acc ? 1 : 0) | (race ? 2 : 0) | (valid ? 0 : 4));
+    }
+    __syncthreads();
+    const int flags = __float_as_int(s_dec[2]);
+    const bool acc = flags & 1, race = flags & 2;
+    const bool resid = has_q && !acc;
+    const uint64_t rkey = stream_key(P.seed, P.req_offset + b, i, 1);
+
+    // ---- sweep 2: beta and the race ---------------------------------------
+    float beta = 0.0f;
+    Race best = race_none();
+    if (has_q && race)
+      sweep2<TT, NT, true, true>(row, qrow, V, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+    else if (has_q)
+      sweep2<TT, NT, true, false>(row, qrow, V, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+    else if (race)
+      sweep2<TT, NT, false, true>(row, qrow, V, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+    beta = warp_sum(beta);
+    warp_race(best);
+    if (lane == 0) red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
+    __syncthreads();
+    if (tid == 0) {
+      float bt = 0.0f;
+      Race tb = race_none();
+      for (int w = 0; w < NW; ++w) {
+        const float4 r4 = red[par ^ 1][w];
+        bt += r4.x;
+        race_merge(tb, r4.y, r4.z, __float_as_int(r4.w));
+      }
+      P.row_stats[t] = make_float2(M, S);
+      uint32_t st = kStDone;
+      if (has_q) {
+        if (flags & 4) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+        if (acc) st |= kStAccepted;
+        if (P.out_beta) P.out_beta[d] = bt;
+        if (P.out_px) P.out_px[d] = s_dec[0];
+        if (P.out_qx) P.out_qx[d] = s_dec[1];
+        if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+      }
+      if (race && tb.w > 0.0f) {
+        P.out_tokens[t] = tb.idx;
+        st |= kStRaceDone;
+      }
+      st_relaxed_u64(P.status + t, make_status(P.epoch, st));
+    }
+    // s_slot / s_dec / red[par] are rewritten next iteration only after the
+    // __syncthreads that follows thread 0's next slot grab.
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Two-pass path (T > 0): statistics of every target row, then one block per
+// draft row for beta and the accept test.  Grid-stride loops, so the grid does
+// not depend on N_t (read from cu[B] on the device).
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ void block_softmax(float& m, float& s, float c, float4* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  warp_softmax(m, s, c);
+  __syncthreads();
+  if (lane == 0) red[warp] = make_float4(m, s, 0.f, 0.f);
+  __syncthreads();
+  m = -INFINITY;
+  s = 0.0f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) softmax_merge(m, s, red[w].x, red[w].y, c);
+}
+
+template <typename TT>
+__global__ void __launch_bounds__(kRowThreads) stats_kernel(const Params P) {
+  __shared__ float4 red[kRowThreads / 32];
+  const int B = P.B, V = P.V;
+  const int64_t n_t = (int64_t)__ldg(P.cu + B) + B;
+  const int64_t rows = min(n_t, P.cap_rows);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (n_t > P.cap_rows) set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+    if (P.defer_count) *P.defer_count = 0;
+  }
+  for (int64_t t = blockIdx.x; t < rows; t += gridDim.x) {
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    float m = -INFINITY, s = 0.0f;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float x = load_logit(row + v);
+      if (x > m) {
+        s *= ex2((m - x) * P.c);
+        m = x;
+      }
+      if (m != -INFINITY) s += ex2((x - m) * P.c);
+    }
+    block_softmax<TT>(m, s, P.c, red);
+    if (threadIdx.x == 0) P.row_stats[t] = make_float2(m, s);
+    __syncthreads();
+  }
+}
+
+template <typename TT>
+__global__ void __launch_bounds__(kRowThreads) verify_kernel(const Params P) {
+  __shared__ float red[kRowThreads / 32];
+  const int B = P.B, V = P.V;
+  const int64_t n_d = __ldg(P.cu + B);
+  for (int64_t d = blockIdx.x; d < n_d; d += gridDim.x) {
+    const int b = request_of_draft(P.cu, B, d);
+    const int c0 = __ldg(P.cu + b);
+    const int i = (int)(d - c0);
+    const int64_t t = d + b;
+    if (t >= P.cap_rows || i < 0) continue;
+    const float2 ms = P.row_stats[t];
+    const float invS = 1.0f / ms.y;
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    const float* qrow = P.q + d * (int64_t)V;
+    float beta = 0.0f;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float p = ex2((load_logit(row + v) - ms.x) * P.c) * invS;
+      beta += fminf(p, __ldg(qrow + v));
+    }
+    beta = warp_sum(beta);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = beta;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float bt = 0.0f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) bt += red[w];
+      const int x = __ldg(P.ids + d);
+      const bool valid = (x >= 0 && x < V);
+      float px = 0.0f, qx = 0.0f;
+      if (valid) {
+        px = ex2((load_logit(row + x) - ms.x) * P.c) * invS;
+        qx = __ldg(qrow + x);
+      } else {
+        set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+      }
+      const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
+      const bool acc = accept_test(r, px, qx);
+      if (P.out_beta) P.out_beta[d] = bt;
+      if (P.out_px) P.out_px[d] = px;
+      if (P.out_qx) P.out_qx[d] = qx;
+      if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+      st_relaxed_u64(P.status + t, make_status(P.epoch, kStDone | (acc ? kStAccepted : 0u)));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// First-rejection scan per request (T > 0): n_b, accepted drafts, -1 tail, and
+// the list of requests whose extra token the race kernel still has to draw.
+// ---------------------------------------------------------------------------
+__global__ void finalize_kernel(const Params P) {
+  const int B = P.B;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && P.sched) *P.sched = 0ull;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t0 = (int64_t)c0 + b;
+    if (g < 0 || t0 + g >= P.cap_rows) continue;
+    int n = g;
+    for (int i = 0; i < g; ++i) {
+      const uint64_t st = P.status[t0 + i];
+      if ((st >> 8) != P.epoch || !(st & kStDone)) {  // row never verified (aborted launch)
+        set_err(P.err, SPECDEC_DEVERR_TIMEOUT);
+        n = i;
+        break;
+      }
+      if (!(st & kStAccepted)) {
+        n = i;
+        break;
+      }
+    }
+    P.out_nacc[b] = n;
+    for (int i = 0; i < n; ++i) P.out_tokens[t0 + i] = __ldg(P.ids + c0 + i);
+    for (int i = n + 1; i <= g; ++i) P.out_tokens[t0 + i] = -1;
+    const uint64_t st = P.status[t0 + n];
+    if (!((st >> 8) == P.epoch && (st & kStRaceDone))) {
+      P.ws_nacc[b] = n;
+      const int k = atomicAdd(P.defer_count, 1);
+      P.defer_list[k] = b;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Race for deferred requests: one block per request, re-reads row (b, n_b)
+// (and the draft row when it is a correction).  Falls back to w = p when the
+// residual max(0, p - q) is zero everywhere (only reachable through rounding).
+// ---------------------------------------------------------------------------
+template <typename TT>
+__global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
+  __shared__ float4 red[kRowThreads / 32];
+  const int V = P.V;
+  const int count = *P.defer_count;
+  for (int k = blockIdx.x; k < count; k += gridDim.x) {
+    const int b = P.defer_list[k];
+    const int n = P.ws_nacc[b];
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t = (int64_t)c0 + b + n;
+    const bool has_q = n < g;
+    const float2 ms = P.row_stats[t];
+    const float invS = 1.0f / ms.y;
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    const float* qrow = has_q ? P.q + ((int64_t)c0 + n) * (int64_t)V : nullptr;
+    const uint64_t rkey = stream_key(P.seed, P.req_offset + b, n, 1);
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      const bool resid = has_q && attempt == 0;
+      Race best = race_none();
+      for (int v = threadIdx.x; v < V; v += blockDim.x) {
+        const float p = ex2((load_logit(row + v) - ms.x) * P.c) * invS;
+        race_offer(best, resid ? fmaxf(p - __ldg(qrow + v), 0.0f) : p, rkey, (uint32_t)v);
+      }
+      warp_race(best);
+      __syncthreads();
+      if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = make_float4(best.w, best.e, __int_as_float(best.idx), 0.f);
+      __syncthreads();
+      Race tb = race_none();
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+        race_merge(tb, red[w].x, red[w].y, __float_as_int(red[w].z));
+      if (tb.w > 0.0f) {
+        if (threadIdx.x == 0) P.out_tokens[t] = tb.idx;
+        break;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Greedy path (T == 0).
+// ---------------------------------------------------------------------------
+template <typename TT>
+__global__ void __launch_bounds__(kRowThreads) greedy_partial_kernel(const Params P, int vec_ok) {
+  __shared__ uint64_t red[kRowThreads / 32];
+  const int B = P.B, V = P.V, parts = P.gparts, plen = P.gpart_len;
+  const int64_t n_t = min((int64_t)__ldg(P.cu + B) + B, P.cap_rows);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (int64_t)__ldg(P.cu + B) + B > P.cap_rows)
+    set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+  const int64_t units = n_t * parts;
+  constexpr int kEl = 16 / sizeof(TT);
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t t = u / parts;
+    const int part = (int)(u % parts);
+    const int v0 = part * plen, v1 = min(V, v0 + plen);
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    uint64_t best = 0;
+    if (vec_ok) {
+      for (int e = v0 + threadIdx.x * kEl; e < v1; e += blockDim.x * kEl) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + e));
+        if constexpr (sizeof(TT) == 2) {
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint64_t a = argmax_key(bf16_lo(ws[k]), e + 2 * k);
+            uint64_t c = argmax_key(bf16_hi(ws[k]), e + 2 * k + 1);
+            best = a > best ? a : best;
+            best = c > best ? c : best;
+          }
+        } else {
+          const float f[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                              __uint_as_float(w.w)};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint64_t a = argmax_key(f[k], e + k);
+            best = a > best ? a : best;
+          }
+        }
+      }
+    } else {
+      for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+        uint64_t a = argmax_key(load_logit(row + v), v);
+        best = a > best ? a : best;
+      }
+    }
+    best = warp_max_u64(best);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint64_t bt = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) bt = red[w] > bt ? red[w] : bt;
+      P.gkeys[u] = bt;
+    }
+  }
+}
+
+__global__ void greedy_finalize_kernel(const Params P) {
+  const int B = P.B, V = P.V, parts = P.gparts;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t0 = (int64_t)c0 + b;
+    if (g < 0 || t0 + g >= P.cap_rows) continue;
+    int n = g, tok = -1;
+    for (int i = 0; i <= g; ++i) {
+      uint64_t k = 0;
+      for (int p = 0; p < parts; ++p) {
+        const uint64_t a = P.gkeys[(t0 + i) * parts + p];
+        k = a > k ? a : k;
+      }
+      const int gi = (int)argmax_key_index(k);
+      if (i == g) {
+        if (n == g) tok = gi;
+        break;
+      }
+      const int x = __ldg(P.ids + c0 + i);
+      if (x < 0 || x >= V) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+      const bool acc = (x == gi);
+      const int64_t d = (int64_t)c0 + i;
+      if (P.out_beta) P.out_beta[d] = acc ? 1.0f : 0.0f;
+      if (P.out_px) P.out_px[d] = acc ? 1.0f : 0.0f;
+      if (P.out_qx) P.out_qx[d] = 1.0f;
+      if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+      if (!acc && n == g) {
+        n = i;
+        tok = gi;
+      }
+    }
+    P.out_nacc[b] = n;
+    for (int i = 0; i < n; ++i) P.out_tokens[t0 + i] = __ldg(P.ids + c0 + i);
+    P.out_tokens[t0 + n] = tok;
+    for (int i = n + 1; i <= g; ++i) P.out_tokens[t0 + i] = -1;
+  }
+}
+
+__global__ void uniform_fill_kernel(uint64_t key, uint64_t v0, int64_t n, float* out) {
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+       j += (int64_t)gridDim.x * blockDim.x)
+    out[j] = uniform_from_bits(uniform_bits(key, v0 + (uint64_t)j));
+}
+
+// -E = ln U for U(k) with k given: used by the tests of the log evaluation.
+__global__ void neglog_fill_kernel(uint32_t k0, int64_t n, float* out) {
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+       j += (int64_t)gridDim.x * blockDim.x)
+    out[j] = neg_log_uniform(k0 + (uint32_t)j);
+}
+
+}  // namespace specdec

@@ -1,0 +1,166 @@
+"""Torch-facing wrapper of libspecdec.so: argument marshalling only (every
+step of the verifier runs in the library's CUDA kernels)."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_FUSED,  # noqa: F401
+                   SPECDEC_PATH_GREEDY, SPECDEC_PATH_SWEEP, SPECDEC_PATH_TWO_PASS, specdec_create, specdec_destroy,
+                   specdec_get_error, specdec_last_path, specdec_neg_log_uniform,
+                   specdec_rejection_sample, specdec_rejection_sample_ex, specdec_reserve,
+                   specdec_set_path, specdec_set_timing_events, specdec_status_string,
+                   specdec_uniform)
+
+
+class SpecdecError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        super().__init__(f"{what}: {specdec_status_string(status)} ({status})")
+        self.status = status
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise SpecdecError(rc, what)
+
+
+@dataclass
+class VerifyOutput:
+    tokens: torch.Tensor         # int32 [N_t]
+    num_accepted: torch.Tensor   # int32 [B]
+    beta: torch.Tensor | None    # float32 [N_d]
+    target_prob: torch.Tensor | None = None   # float32 [N_d] p_i(x_i)
+    draft_prob: torch.Tensor | None = None    # float32 [N_d] q_i(x_i)
+    accept: torch.Tensor | None = None        # int32 [N_d]
+
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream_handle(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class Verifier:
+    """One library handle on one CUDA device."""
+
+    def __init__(self, device: int | torch.device = 0):
+        dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        if dev.type != "cuda":
+            raise ValueError("the verifier runs on a CUDA device")
+        self.device = dev
+        idx = dev.index if dev.index is not None else torch.cuda.current_device()
+        rc, self._h = specdec_create(idx)
+        _check(rc, "specdec_create")
+
+    def close(self):
+        if getattr(self, "_h", 0):
+            specdec_destroy(self._h)
+            self._h = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self) -> int:
+        return self._h
+
+    def reserve(self, max_draft_positions: int, max_batch: int):
+        _check(specdec_reserve(self._h, max_draft_positions, max_batch), "specdec_reserve")
+
+    def set_timing_events(self, before_rows, after_rows):
+        """torch.cuda.Event pair (already recorded once, so that the CUDA event
+        exists) recorded around the row kernel of every later call; None, None
+        to stop."""
+        a = None if before_rows is None else before_rows.cuda_event
+        b = None if after_rows is None else after_rows.cuda_event
+        _check(specdec_set_timing_events(self._h, a, b), "specdec_set_timing_events")
+
+    def set_path(self, path: int):
+        _check(specdec_set_path(self._h, path), "specdec_set_path")
+
+    def last_path(self) -> tuple[int, int]:
+        rc, p, c = specdec_last_path(self._h)
+        _check(rc, "specdec_last_path")
+        return p, c
+
+    def get_error(self) -> int:
+        rc, e = specdec_get_error(self._h, _stream_handle(self.device))
+        _check(rc, "specdec_get_error")
+        return e
+
+    def __call__(self, target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
+                 draft_ids: torch.Tensor, cu_num_draft_tokens: torch.Tensor, T: float, seed: int,
+                 *, with_beta: bool = True, extended: bool = False,
+                 out: VerifyOutput | None = None, n_draft: int | None = None,
+                 request_offset: int = 0) -> VerifyOutput:
+        """Runs one verify step on the current torch stream.  ``n_draft`` (= cu[B])
+        avoids a host read of cu when output tensors must be allocated."""
+        for t in (target_logits, draft_ids, cu_num_draft_tokens):
+            if t.device != self.device or not t.is_contiguous():
+                raise ValueError("inputs must be contiguous tensors on the verifier's device")
+        if draft_probs is not None and (draft_probs.device != self.device
+                                        or draft_probs.dtype != torch.float32
+                                        or not draft_probs.is_contiguous()):
+            raise ValueError("draft_probs must be a contiguous float32 tensor on the device")
+        if target_logits.dtype == torch.float32:
+            dtype = SPECDEC_F32
+        elif target_logits.dtype == torch.bfloat16:
+            dtype = SPECDEC_BF16
+        else:
+            raise TypeError("target_logits must be float32 or bfloat16")
+        if draft_ids.dtype != torch.int32 or cu_num_draft_tokens.dtype != torch.int32:
+            raise TypeError("draft_ids and cu_num_draft_tokens must be int32")
+        B = cu_num_draft_tokens.numel() - 1
+        V = target_logits.shape[-1]
+        if out is None:
+            nd = int(cu_num_draft_tokens[-1]) if n_draft is None else int(n_draft)
+            kw = dict(device=self.device)
+            out = VerifyOutput(
+                tokens=torch.empty(nd + B, dtype=torch.int32, **kw),
+                num_accepted=torch.empty(B, dtype=torch.int32, **kw),
+                beta=torch.empty(nd, dtype=torch.float32, **kw) if with_beta else None)
+            if extended:
+                out.target_prob = torch.empty(nd, dtype=torch.float32, **kw)
+                out.draft_prob = torch.empty(nd, dtype=torch.float32, **kw)
+                out.accept = torch.empty(nd, dtype=torch.int32, **kw)
+        stream = _stream_handle(self.device)
+        if (out.target_prob is not None or out.draft_prob is not None or out.accept is not None
+                or request_offset):
+            rc = specdec_rejection_sample_ex(
+                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),
+                _ptr(cu_num_draft_tokens), B, V, float(T), int(seed), int(request_offset),
+                _ptr(out.tokens),
+                _ptr(out.num_accepted), _ptr(out.beta), _ptr(out.target_prob),
+                _ptr(out.draft_prob), _ptr(out.accept), stream)
+        else:
+            rc = specdec_rejection_sample(
+                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),
+                _ptr(cu_num_draft_tokens), B, V, float(T), int(seed), _ptr(out.tokens),
+                _ptr(out.num_accepted), _ptr(out.beta), stream)
+        _check(rc, "specdec_rejection_sample")
+        return out
+
+
+def uniform(seed: int, b: int, pos: int, stream_id: int, v0: int, n: int,
+            device: int | torch.device = 0) -> torch.Tensor:
+    """The generator's uniforms U(seed, b, pos, stream_id, v0 .. v0+n-1) (float32)."""
+    dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    _check(specdec_uniform(seed, b, pos, stream_id, v0, n, out.data_ptr(), _stream_handle(dev)),
+           "specdec_uniform")
+    return out
+
+
+def neg_log_uniform(k0: int, n: int, device: int | torch.device = 0) -> torch.Tensor:
+    dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    _check(specdec_neg_log_uniform(k0, n, out.data_ptr(), _stream_handle(dev)),
+           "specdec_neg_log_uniform")
+    return out

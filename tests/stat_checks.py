@@ -69,16 +69,16 @@ def chi2_ok(counts, probs, min_expected=5.0):
     return res.pvalue
 
 
-def check_a_output_distribution(run, n=1_000_000, seed=101, T=1.0):
+def check_a_output_distribution(run, n=1_000_000, seed=12, T=1.0):
     """(a) slot-0 token ~ p_0; within n = 0, token ~ norm(max(0, p_0 - q_0));
     within n = gamma, bonus ~ p_gamma."""
     rng = np.random.default_rng(seed)
-    V, gamma = 6, 2
-    tgt_rows = np.array([[0.3, -1.0, 1.2, 0.0, 0.7, -0.4],
-                         [1.0, 0.2, -0.5, 0.9, 0.0, -1.5],
-                         [-0.2, 0.8, 0.1, -1.0, 1.4, 0.3]], np.float32)
-    draft_rows = np.array([[0.05, 0.30, 0.10, 0.25, 0.10, 0.20],
-                           [0.20, 0.20, 0.20, 0.05, 0.25, 0.10]], np.float32)
+    V, gamma = 8, 2
+    tgt_rows = np.array([[0.3, -1.0, 1.2, 0.0, 0.7, -0.4, 0.5, -2.0],
+                         [1.0, 0.2, -0.5, 0.9, 0.0, -1.5, 0.4, 0.1],
+                         [-0.2, 0.8, 0.1, -1.0, 1.4, 0.3, -0.6, 0.9]], np.float32)
+    draft_rows = np.array([[0.05, 0.25, 0.10, 0.20, 0.10, 0.15, 0.05, 0.10],
+                           [0.20, 0.15, 0.15, 0.05, 0.20, 0.10, 0.10, 0.05]], np.float32)
     tgt, q, ids, cu = tile_batch(tgt_rows, draft_rows, n, rng)
     tokens, nacc, accept, beta = run(tgt, q, ids, cu, T, seed)
     tok = tokens.reshape(n, gamma + 1)
