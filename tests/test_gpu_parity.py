@@ -216,6 +216,7 @@ def test_single_request_bonus_only(V):
                        num_accepted=torch.empty(1, dtype=torch.int32, device="cuda"), beta=None)
     V(wd.target_logits, wd.draft_probs, ids, wd.cu, w.T, w.seed, out=out)
     g = dict(tokens=out.tokens.cpu().numpy(), num_accepted=out.num_accepted.cpu().numpy())
+    w = from_rows(t, torch.zeros(0, 4096), torch.zeros(0, dtype=torch.int32), [0], T=1.0, seed=5)
     r = run_oracle(w)
     assert g["num_accepted"][0] == 0 and g["tokens"][0] == r.tokens[0]
 
