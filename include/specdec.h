@@ -178,6 +178,37 @@ int specdec_uniform(uint64_t seed, uint64_t b, uint64_t pos, uint32_t stream_id,
  * race uses (so tests can bound its error against double precision). */
 int specdec_neg_log_uniform(uint32_t k0, int64_t n, float* out, void* stream);
 
+/* ---- allocation-free variant -----------------------------------------------
+ * No counterpart in the paper: this entry point exists for callers that cannot
+ * allocate device memory at the point where they verify (code running inside a
+ * memory pool or arena it does not own, plug-ins that are handed only
+ * pre-allocated buffers, hosts that freeze device allocation after start-up).
+ * It needs no handle and allocates nothing: its scratch (per-row softmax
+ * statistics and status words, the deferred-request list, a few counters) is
+ * one file-scope device array of about 2.4 MB, which every GPU that loads the
+ * library holds until the process exits.  It runs the same kernels as
+ * specdec_rejection_sample (the sweep path for T > 0, the greedy path at
+ * T == 0) with the same arguments, plus:
+ *   n_draft_positions  cu[B] (the host needs it to check the size limits)
+ *   out_device_error   optional device word; SPECDEC_DEVERR_* bits are OR-ed
+ *                      into it (the caller clears it); NULL drops them
+ * Limits: cu[B] + B <= SPECDEC_NOALLOC_MAX_ROWS and B <= SPECDEC_NOALLOC_MAX_BATCH;
+ * larger calls return SPECDEC_ERR_CAPACITY before anything is queued.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it: make that first call before any stream
+ * capture.  Every call on a device shares the one array and it keeps the last
+ * call's contents; each call clears the counters it needs at its start, on its
+ * stream.  Calls whose work overlaps on the GPU (two streams, two host threads)
+ * race on the array and must be serialised by the caller. */
+#define SPECDEC_NOALLOC_MAX_ROWS 16384
+#define SPECDEC_NOALLOC_MAX_BATCH 4096
+int specdec_rejection_sample_noalloc(const void* target_logits, int dtype,
+                                     const float* draft_probs, const int32_t* draft_ids,
+                                     const int32_t* cu_num_draft_tokens, int B, int V, float T,
+                                     uint64_t seed, int64_t n_draft_positions,
+                                     int32_t* out_tokens, int32_t* out_num_accepted,
+                                     float* out_beta, uint32_t* out_device_error, void* stream);
+
 /* Human-readable text of a status code (static storage). */
 const char* specdec_status_string(int status);
 

@@ -29,6 +29,9 @@ SPECDEC_DEVERR_BAD_CU = 2
 SPECDEC_DEVERR_CAPACITY = 4
 SPECDEC_DEVERR_TIMEOUT = 8
 
+SPECDEC_NOALLOC_MAX_ROWS = 16384
+SPECDEC_NOALLOC_MAX_BATCH = 4096
+
 SPECDEC_PATH_AUTO = 0
 SPECDEC_PATH_FUSED = 1
 SPECDEC_PATH_TWO_PASS = 2
@@ -65,6 +68,8 @@ _set_events = _fn("specdec_set_timing_events", _i32, _vp, _vp, _vp)
 _last_path = _fn("specdec_last_path", _i32, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
 _uniform = _fn("specdec_uniform", _i32, _u64, _u64, _u64, _u32, _u64, _i64, _vp, _vp)
 _neg_log = _fn("specdec_neg_log_uniform", _i32, _u32, _i64, _vp, _vp)
+_rs_noalloc = _fn("specdec_rejection_sample_noalloc", _i32, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
+                  _f32, _u64, _i64, _vp, _vp, _vp, _vp, _vp)
 _status_string = _fn("specdec_status_string", ctypes.c_char_p, _i32)
 _destroy = _fn("specdec_destroy", _i32, _vp)
 
@@ -122,6 +127,15 @@ def specdec_neg_log_uniform(k0, n, out, stream) -> int:
     return _neg_log(k0, n, out, stream)
 
 
+def specdec_rejection_sample_noalloc(target_logits, dtype, draft_probs, draft_ids,
+                                     cu_num_draft_tokens, B, V, T, seed, n_draft_positions,
+                                     out_tokens, out_num_accepted, out_beta, out_device_error,
+                                     stream) -> int:
+    return _rs_noalloc(target_logits, dtype, draft_probs, draft_ids, cu_num_draft_tokens, B, V, T,
+                       seed & 0xFFFFFFFFFFFFFFFF, n_draft_positions, out_tokens, out_num_accepted,
+                       out_beta, out_device_error, stream)
+
+
 def specdec_status_string(status: int) -> str:
     return _status_string(status).decode()
 
@@ -134,4 +148,4 @@ EXPORTED = ["specdec_create", "specdec_reserve", "specdec_rejection_sample",
             "specdec_rejection_sample_ex", "specdec_get_error", "specdec_set_path",
             "specdec_set_timing_events",
             "specdec_last_path", "specdec_uniform", "specdec_neg_log_uniform",
-            "specdec_status_string", "specdec_destroy"]
+            "specdec_rejection_sample_noalloc", "specdec_status_string", "specdec_destroy"]

@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libspecdec.so")
-SOURCES = ["specdec.cu"]
+SOURCES = ["specdec.cu", "noalloc.cu"]
 HEADERS = ["device_common.cuh", "kernels.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

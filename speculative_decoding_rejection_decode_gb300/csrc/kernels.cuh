@@ -21,6 +21,9 @@
 // timinsight guide's Step 2 pseudo-code; beta from Theorem 3.5.
 #pragma once
 
+// Non-template kernels are `static`: each translation unit that launches them
+// (the handle path and the allocation-free path) keeps its own copy.
+
 #include "device_common.cuh"
 
 namespace specdec {
@@ -819,7 +822,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(const Params P) {
 // First-rejection scan per request (T > 0): n_b, accepted drafts, -1 tail, and
 // the list of requests whose extra token the race kernel still has to draw.
 // ---------------------------------------------------------------------------
-__global__ void finalize_kernel(const Params P) {
+static __global__ void finalize_kernel(const Params P) {
   const int B = P.B;
   if (blockIdx.x == 0 && threadIdx.x == 0 && P.sched) *P.sched = 0ull;
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
@@ -954,7 +957,7 @@ __global__ void __launch_bounds__(kRowThreads) greedy_partial_kernel(const Param
   }
 }
 
-__global__ void greedy_finalize_kernel(const Params P) {
+static __global__ void greedy_finalize_kernel(const Params P) {
   const int B = P.B, V = P.V, parts = P.gparts;
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
     const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
@@ -992,14 +995,14 @@ __global__ void greedy_finalize_kernel(const Params P) {
   }
 }
 
-__global__ void uniform_fill_kernel(uint64_t key, uint64_t v0, int64_t n, float* out) {
+static __global__ void uniform_fill_kernel(uint64_t key, uint64_t v0, int64_t n, float* out) {
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
        j += (int64_t)gridDim.x * blockDim.x)
     out[j] = uniform_from_bits(uniform_bits(key, v0 + (uint64_t)j));
 }
 
 // -E = ln U for U(k) with k given: used by the tests of the log evaluation.
-__global__ void neglog_fill_kernel(uint32_t k0, int64_t n, float* out) {
+static __global__ void neglog_fill_kernel(uint32_t k0, int64_t n, float* out) {
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
        j += (int64_t)gridDim.x * blockDim.x)
     out[j] = neg_log_uniform(k0 + (uint32_t)j);

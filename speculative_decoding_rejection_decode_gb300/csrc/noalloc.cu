@@ -1,0 +1,155 @@
+// Allocation-free entry point: specdec_rejection_sample_noalloc.
+//
+// Some callers cannot call cudaMalloc at the point where they verify: code that
+// runs inside a memory pool or arena they do not own, plug-ins that are given
+// only pre-allocated buffers, or hosts that forbid device allocation after
+// start-up so that memory use stays fixed.  For them this entry point runs the
+// same kernels as specdec_rejection_sample, but its scratch (per-row softmax
+// statistics and status words, the deferred-request list and a few counters)
+// lives in one file-scope __device__ array of fixed size instead of a
+// handle-owned allocation.  Every GPU that loads the library holds that array
+// until the process exits.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.cuh"
+
+using namespace specdec;
+
+namespace {
+
+constexpr int64_t kRows = SPECDEC_NOALLOC_MAX_ROWS;
+constexpr int kBatch = SPECDEC_NOALLOC_MAX_BATCH;
+constexpr int kParts = 16;  // greedy argmax slices per row, as in the handle path
+constexpr int kThreads = 1024;
+
+constexpr size_t kStatsOff = 0;
+constexpr size_t kStatusOff = kStatsOff + kRows * sizeof(float2);
+constexpr size_t kKeysOff = kStatusOff + kRows * sizeof(uint64_t);
+constexpr size_t kNaccOff = kKeysOff + kRows * kParts * sizeof(uint64_t);
+constexpr size_t kListOff = kNaccOff + kBatch * sizeof(int32_t);
+constexpr size_t kSmallOff = kListOff + kBatch * sizeof(int32_t);  // err, defer count, counter
+constexpr size_t kSmallBytes = 64;
+constexpr size_t kScratchBytes = kSmallOff + kSmallBytes;
+static_assert(kStatusOff % 256 == 0 && kKeysOff % 256 == 0 && kNaccOff % 256 == 0 &&
+                  kListOff % 256 == 0 && kSmallOff % 256 == 0,
+              "scratch sections stay 256-byte aligned");
+
+}  // namespace
+
+// The scratch array.  In host code this name is only a stand-in: its device
+// address comes from cudaGetSymbolAddress, taken once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+std::atomic<uint64_t> g_epoch{0};
+
+// Device address of the scratch array on the current device (set up on the
+// first call per device).
+int scratch_on_current_device(unsigned char** out, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPECDEC_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return SPECDEC_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
+  return SPECDEC_OK;
+}
+
+}  // namespace
+
+extern "C" int specdec_rejection_sample_noalloc(
+    const void* target_logits, int dtype, const float* draft_probs, const int32_t* draft_ids,
+    const int32_t* cu_num_draft_tokens, int B, int V, float T, uint64_t seed,
+    int64_t n_draft_positions, int32_t* out_tokens, int32_t* out_num_accepted, float* out_beta,
+    uint32_t* out_device_error, void* stream) {
+  if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED_DTYPE;
+  if (B <= 0 || V <= 0 || V > (1 << 30) || n_draft_positions < 0) return SPECDEC_ERR_INVALID_ARG;
+  if (!std::isfinite(T) || T < 0.0f) return SPECDEC_ERR_INVALID_ARG;
+  if (!target_logits || !draft_ids || !cu_num_draft_tokens || !out_tokens || !out_num_accepted)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (T > 0.0f && !draft_probs) return SPECDEC_ERR_INVALID_ARG;
+  if (B > kBatch || n_draft_positions + B > kRows) return SPECDEC_ERR_CAPACITY;
+
+  unsigned char* base = nullptr;
+  int sms = 0;
+  int rc = scratch_on_current_device(&base, &sms);
+  if (rc != SPECDEC_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* small = reinterpret_cast<uint32_t*>(base + kSmallOff);
+  // Counters left by an earlier call (or by an earlier call that failed part-way)
+  // must start at zero; status words need no clearing (each call has its epoch).
+  if (cudaMemsetAsync(small, 0, kSmallBytes, st) != cudaSuccess) return SPECDEC_ERR_CUDA;
+
+  Params P = {};
+  P.logits = target_logits;
+  P.q = draft_probs;
+  P.ids = draft_ids;
+  P.cu = cu_num_draft_tokens;
+  P.B = B;
+  P.V = V;
+  P.c = T > 0.0f ? kLog2e / T : 0.0f;
+  P.seed = seed;
+  P.req_offset = 0;
+  P.epoch = ++g_epoch;
+  P.out_tokens = out_tokens;
+  P.out_nacc = out_num_accepted;
+  P.out_beta = out_beta;
+  P.row_stats = reinterpret_cast<float2*>(base + kStatsOff);
+  P.status = reinterpret_cast<uint64_t*>(base + kStatusOff);
+  P.gkeys = reinterpret_cast<uint64_t*>(base + kKeysOff);
+  P.ws_nacc = reinterpret_cast<int32_t*>(base + kNaccOff);
+  P.defer_list = reinterpret_cast<int32_t*>(base + kListOff);
+  P.err = out_device_error ? out_device_error : small;
+  P.defer_count = reinterpret_cast<int32_t*>(small + 1);
+  P.sched = reinterpret_cast<unsigned long long*>(small + 2);
+  P.cap_rows = kRows;
+  P.cap_b = kBatch;
+
+  const int esize = dtype == SPECDEC_BF16 ? 2 : 4;
+  if (T == 0.0f) {
+    int parts = (int)std::min<int64_t>(kParts, std::max<int64_t>(1, (V + 16383) / 16384));
+    const int plen = (int)(((V + parts - 1) / parts + 7) / 8 * 8);
+    parts = (V + plen - 1) / plen;
+    P.gparts = parts;
+    P.gpart_len = plen;
+    const int vec_ok = ((int64_t)V * esize) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(target_logits) % 16 == 0;
+    if (dtype == SPECDEC_BF16)
+      greedy_partial_kernel<__nv_bfloat16><<<sms * 8, kRowThreads, 0, st>>>(P, vec_ok);
+    else
+      greedy_partial_kernel<float><<<sms * 8, kRowThreads, 0, st>>>(P, vec_ok);
+    greedy_finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
+  } else {
+    P.vec_ok = ((int64_t)V * esize) % 16 == 0 && ((int64_t)V * 4) % 16 == 0 &&
+               reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
+               reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
+    const int race_grid = std::max(1, std::min(B, sms * 4));
+    if (dtype == SPECDEC_BF16) {
+      sweep_row_kernel<__nv_bfloat16, kThreads><<<sms, kThreads, 0, st>>>(P);
+      finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
+      race_kernel<__nv_bfloat16><<<race_grid, kRowThreads, 0, st>>>(P);
+    } else {
+      sweep_row_kernel<float, kThreads><<<sms, kThreads, 0, st>>>(P);
+      finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
+      race_kernel<float><<<race_grid, kRowThreads, 0, st>>>(P);
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
