@@ -37,7 +37,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["speculative_decoding_rejection_decode_gb300/csrc/kernels.cuh",
                   "speculative_decoding_rejection_decode_gb300/csrc/device_common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_row_kernel_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "row_kernel_traffic_large_workload.txt")
 
 
 def parse_args():
@@ -164,7 +164,7 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_key: str):
+def recorded_traffic(workload_key: str, kernel: str):
     """DRAM bytes per launch of the row kernel from the committed ncu summary,
     when it was taken on the current kernel source and this workload."""
     try:
@@ -175,7 +175,7 @@ def recorded_traffic(workload_key: str):
                 vals[k.strip()] = v.strip()
         if vals.get("source_sha256_16") != kernel_source_hash():
             return None
-        if vals.get("workload_key") != workload_key:
+        if vals.get("workload_key") != workload_key or vals.get("kernel") != kernel:
             return None
         return float(vals["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -321,7 +321,7 @@ def main():
     row_avg_ms = statistics.mean(row_ms)
     peak, peak_kind = measured_peak_gbs()
     achieved = alg_bytes_rows / (row_avg_ms / 1e3) / 1e9
-    traffic = recorded_traffic(workload_key)
+    traffic = recorded_traffic(workload_key, kernel_name)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
