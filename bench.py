@@ -344,6 +344,15 @@ def main():
         "wall_s_timed_region": t_wall,
     }
 
+    nacc = out.num_accepted.double()
+    result["acceptance"] = {
+        # accepted drafts / proposed drafts (the timinsight guide's definition)
+        "draft_acceptance_rate": float(nacc.sum()) / max(w.n_draft, 1),
+        # 1 + accepted per verify step and request (vLLM's mean acceptance length; Eq. (1)'s E[N])
+        "mean_acceptance_length": 1.0 + float(nacc.mean()),
+        # alpha = E[beta] (Corollary 3.6)
+        "alpha_mean_beta": float(out.beta.double().mean()),
+    }
     if not args.no_e2e:
         result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
