@@ -40,9 +40,9 @@
  * draft_probs [N_d, V].
  *
  * Ownership: the caller owns every input and output buffer (device memory).  The
- * handle owns a device workspace (per-row softmax statistics and status words,
- * about 24 bytes per target row plus 8 bytes per request) and one stream-ordered
- * error word.  A handle serves one stream at a time; calls on it are
+ * handle owns a device workspace (per-row softmax statistics, status words and
+ * greedy partial keys, 144 bytes per target row, plus 268 bytes per request) and
+ * one stream-ordered error word.  A handle serves one stream at a time; calls on it are
  * asynchronous and never synchronise, except the first call that needs a larger
  * workspace than specdec_reserve() provided (it reads cu[B] back to size it).
  *
@@ -90,6 +90,8 @@ typedef struct specdec_ctx* specdec_handle_t;
 #define SPECDEC_PATH_TWO_PASS 2 /* statistics kernel, then verify kernel (T > 0)     */
 #define SPECDEC_PATH_SWEEP 3    /* one CTA per row pair, second sweep from L2 (T > 0) */
 #define SPECDEC_PATH_GREEDY 4   /* reported by specdec_last_path for T == 0          */
+#define SPECDEC_PATH_STREAM 5   /* the two sweeps fed by bulk copies through a shared-
+                                   memory ring (T > 0; needs 16-byte aligned rows)   */
 
 /* Creates a handle bound to CUDA device `device`.  *out receives the handle.
  * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (null out, bad device) or
@@ -152,9 +154,10 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
  * SPECDEC_ERR_CUDA. */
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream);
 
-/* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP or
- * _AUTO, the default).  A forced FUSED path falls back to SWEEP where its layout
- * rules (16-byte aligned rows, a vocabulary that fits a cluster) do not hold. */
+/* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
+ * _STREAM or _AUTO, the default, which takes SWEEP).  A forced FUSED or STREAM
+ * path falls back to SWEEP where its layout rules (16-byte aligned rows; for
+ * FUSED a vocabulary that fits a cluster) do not hold. */
 int specdec_set_path(specdec_handle_t h, int path);
 
 /* Profiling hook: when set, every later call records `before_rows`
@@ -163,8 +166,8 @@ int specdec_set_path(specdec_handle_t h, int path);
  * Pass NULL, NULL to stop.  The events stay owned by the caller. */
 int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after_rows);
 
-/* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP
- * or _GREEDY), and the cluster size of the fused path (0 otherwise). */
+/* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
+ * _STREAM or _GREEDY), and the cluster size of the fused path (0 otherwise). */
 int specdec_last_path(specdec_handle_t h, int* path, int* cluster_size);
 
 /* Writes out[j] = U(seed, b, pos, stream_id, v0 + j) for j < n into device
@@ -185,7 +188,7 @@ int specdec_neg_log_uniform(uint32_t k0, int64_t n, float* out, void* stream);
  * pre-allocated buffers, hosts that freeze device allocation after start-up).
  * It needs no handle and allocates nothing: its scratch (per-row softmax
  * statistics and status words, the deferred-request list, a few counters) is
- * one file-scope device array of about 2.4 MB, which every GPU that loads the
+ * one file-scope device array of about 3.5 MB, which every GPU that loads the
  * library holds until the process exits.  It runs the same kernels as
  * specdec_rejection_sample (the sweep path for T > 0, the greedy path at
  * T == 0) with the same arguments, plus:

@@ -37,6 +37,7 @@ SPECDEC_PATH_FUSED = 1
 SPECDEC_PATH_TWO_PASS = 2
 SPECDEC_PATH_SWEEP = 3
 SPECDEC_PATH_GREEDY = 4
+SPECDEC_PATH_STREAM = 5
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

@@ -55,6 +55,10 @@ struct Params {
   int32_t* ws_nacc;        // [cap_B] n_b for the race kernel
   int32_t* defer_list;     // [cap_B]
   int32_t* defer_count;    // [1]
+  float4* rpart;           // [cap_B * kRaceMaxSlices] partial race winners per deferred request
+  int32_t* rcount;         // [cap_B] slices finished per deferred request (reset by the last one)
+  int rslices;             // slices per deferred row
+  int rslice_len;          // elements per slice (multiple of 8)
   unsigned long long* sched;  // [1] next work slot of the sweep kernel (reset by finalize)
   uint32_t* err;           // [1] sticky device error word
   int64_t cap_rows;
@@ -69,6 +73,7 @@ struct Params {
 };
 
 constexpr int kChunk = 4096;          // elements per bulk copy / pipeline step
+constexpr int kRaceMaxSlices = 16;    // a deferred row is split over at most this many CTAs
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kFusedThreads = kConsumers + 32;  // + one producer warp
@@ -547,8 +552,8 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
   }
 }
 
-template <typename TT, int NT>
-__global__ void __launch_bounds__(NT, 1) sweep_row_kernel(const Params P) {
+template <typename TT, int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
   constexpr int NW = NT / 32;
   constexpr int kEl = 16 / sizeof(TT);
   __shared__ float4 red[2][NW];
@@ -672,7 +677,9 @@ __global__ void __launch_bounds__(NT, 1) sweep_row_kernel(const Params P) {
         const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
         acc = accept_test(r, px, qx);
       }
-      const bool race = (prefix == kPrefixAllAccepted) && (!has_q || !acc);
+      // the earlier rows may have finished during sweep 1
+      const int pfx = (prefix == kPrefixUnknown) ? read_prefix(P.status, t - i, i, P.epoch) : prefix;
+      const bool race = (pfx == kPrefixAllAccepted) && (!has_q || !acc);
       s_dec[0] = px;
       s_dec[1] = qx;
       s_dec[2] = __int_as_float((acc ? 1 : 0) | (race ? 2 : 0) | (valid ? 0 : 4));
@@ -722,6 +729,322 @@ __global__ void __launch_bounds__(NT, 1) sweep_row_kernel(const Params P) {
     }
     // s_slot / s_dec / red[par] are rewritten next iteration only after the
     // __syncthreads that follows thread 0's next slot grab.
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Streamed row kernel (T > 0): the sweep kernel's two sweeps, fed by bulk copies
+// through a shared-memory ring instead of register-held loads.  One CTA per SM:
+// a producer thread takes work slots (position-major, global counter), publishes
+// a row descriptor and issues, in a fixed order, the 16 KB stages of sweep 1
+// (target row, L2 evict_last) and of sweep 2 (target row again from L2 plus the
+// draft row, evict_first); it runs ahead across rows as far as the ring allows.
+// Sixteen consumer warps follow the same order.  Their reductions and decisions
+// between sweeps do not stop the copies, so HBM keeps streaming.
+// ---------------------------------------------------------------------------
+constexpr int kStreamConsumerWarps = 16;
+constexpr int kStreamConsumers = kStreamConsumerWarps * 32;
+constexpr int kStreamThreads = kStreamConsumers + 32;
+constexpr int kStageBytes = 16384;
+constexpr int kMaxStages = 16;
+constexpr int kDescSlots = 4;
+
+struct alignas(16) StreamShared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t dfull[kDescSlots];
+  uint64_t dempty[kDescSlots];
+  long long desc_u[kDescSlots];     // work slot, or -1 = no more work
+  int desc_prefix[kDescSlots];      // prefix state read when the slot was taken
+  float4 red[2][kStreamConsumerWarps];
+  float dec[4];
+  int gmax, bad;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ bool stream_wait(StreamShared& S, uint32_t bar, uint32_t parity) {
+  if (S.abort_flag) return false;
+  if (mbar_wait(bar, parity)) return true;
+  S.abort_flag = 1;
+  return false;
+}
+
+template <typename TT, int MINB>
+__global__ void __launch_bounds__(kStreamThreads, MINB) stream_row_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  constexpr int kEl1 = kStageBytes / sizeof(TT);  // target elements per stage
+  constexpr int kQPerGroup = kEl1 / 4096;         // draft stages per sweep-2 group (2 bf16, 1 f32)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = P.B, V = P.V;
+  const int NS = P.nq;
+  unsigned char* ring = smem_raw;
+  StreamShared& S = *reinterpret_cast<StreamShared*>(smem_raw + (size_t)NS * kStageBytes);
+  const int n1 = (V + kEl1 - 1) / kEl1;                   // target stages per sweep
+  const int nq = (V + 4095) / 4096;                       // draft stages per row
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&S.full[s]), 1);
+      mbar_init(smem_addr(&S.empty[s]), kStreamConsumerWarps);
+    }
+    for (int s = 0; s < kDescSlots; ++s) {
+      mbar_init(smem_addr(&S.dfull[s]), 1);
+      mbar_init(smem_addr(&S.dempty[s]), 1);
+    }
+    S.gmax = 0;
+    S.bad = 0;
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  {
+    int gm = 0, bad = 0;
+    for (int b = tid; b < B; b += blockDim.x) {
+      const int g = __ldg(P.cu + b + 1) - __ldg(P.cu + b);
+      gm = max(gm, g);
+      bad |= (g < 0);
+    }
+    if (gm) atomicMax(&S.gmax, gm);
+    if (bad) atomicOr(&S.bad, 1);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tid == 0) {
+    if (S.bad || __ldg(P.cu) != 0) set_err(P.err, SPECDEC_DEVERR_BAD_CU);
+    *P.defer_count = 0;
+  }
+  const int64_t total = (int64_t)B * (S.gmax + 1);
+
+  if (warp == kStreamConsumerWarps) {
+    // ===================== producer ==========================================
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+      uint32_t fill = 0, k = 0;
+      auto issue = [&](const void* src, int bytes, uint64_t pol) -> bool {
+        const int s = fill % NS;
+        if (!stream_wait(S, smem_addr(&S.empty[s]), ((fill / NS) & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(smem_addr(&S.full[s]), bytes);
+        bulk_load(smem_addr(ring + (size_t)s * kStageBytes), src, bytes, smem_addr(&S.full[s]), pol);
+        ++fill;
+        return true;
+      };
+      for (;; ++k) {
+        long long u;
+        int prefix = kPrefixAllAccepted;
+        while (true) {
+          u = (long long)atomicAdd(P.sched, 1ull);
+          if (u >= total) {
+            u = -1;
+            break;
+          }
+          const int i = (int)(u / B), b = (int)(u % B);
+          const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+          if (i > g) continue;
+          const int64_t t = (int64_t)c0 + b + i;
+          if (t >= P.cap_rows) {
+            set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+            continue;
+          }
+          prefix = i > 0 ? read_prefix(P.status, t - i, i, P.epoch) : kPrefixAllAccepted;
+          if (i == g && prefix == kPrefixUnknown) {
+            // A bonus row is needed only when every draft was accepted: give the
+            // rows still in flight (on other SMs, never blocked) a bounded time.
+            const uint64_t t0 = globaltimer_ns();
+            while (prefix == kPrefixUnknown && globaltimer_ns() - t0 < 200000ull) {
+              __nanosleep(500);
+              prefix = read_prefix(P.status, t - i, i, P.epoch);
+            }
+          }
+          if (i == g && prefix == kPrefixRejected) continue;  // bonus row nobody needs
+          break;
+        }
+        const int ds = k % kDescSlots;
+        if (!stream_wait(S, smem_addr(&S.dempty[ds]), ((k / kDescSlots) & 1) ^ 1)) u = -1;
+        S.desc_u[ds] = S.abort_flag ? -1 : u;
+        S.desc_prefix[ds] = prefix;
+        mbar_arrive(smem_addr(&S.dfull[ds]));
+        if (u < 0 || S.abort_flag) break;
+        const int i = (int)(u / B), b = (int)(u % B);
+        const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+        const int64_t t = (int64_t)c0 + b + i, d = (int64_t)c0 + i;
+        const bool has_q = i < g;
+        const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+        const float* qrow = P.q + d * (int64_t)V;
+        bool ok = true;
+        for (int c = 0; c < n1 && ok; ++c)
+          ok = issue(row + (size_t)c * kEl1, min(kEl1, V - c * kEl1) * (int)sizeof(TT), keep);
+        for (int c = 0; c < n1 && ok; ++c) {
+          ok = issue(row + (size_t)c * kEl1, min(kEl1, V - c * kEl1) * (int)sizeof(TT), drop);
+          if (has_q)
+            for (int h = 0; h < kQPerGroup && ok; ++h) {
+              const int qc = c * kQPerGroup + h;
+              if (qc < nq) ok = issue(qrow + (size_t)qc * 4096, min(4096, V - qc * 4096) * 4, drop);
+            }
+        }
+        if (!ok) break;
+      }
+      if (S.abort_flag) {
+        set_err(P.err, SPECDEC_DEVERR_TIMEOUT);
+        // let every issued copy land before the CTA may exit
+        for (uint32_t f = fill > (uint32_t)NS ? fill - NS : 0; f < fill; ++f)
+          mbar_wait(smem_addr(&S.full[f % NS]), (f / NS) & 1);
+        for (int s = 0; s < kDescSlots; ++s) {  // release consumers waiting for a row
+          S.desc_u[s] = -1;
+          mbar_arrive(smem_addr(&S.dfull[s]));
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ===================== consumers ===========================================
+  uint32_t cc = 0;
+  for (uint32_t k = 0;; ++k) {
+    const int ds = k % kDescSlots;
+    bool ok = stream_wait(S, smem_addr(&S.dfull[ds]), (k / kDescSlots) & 1);
+    const long long u = ok ? S.desc_u[ds] : -1;
+    const int prefix0 = S.desc_prefix[ds];
+    if (named_bar_or(1, kStreamConsumers, u < 0)) break;
+    const int i = (int)(u / B), b = (int)(u % B);
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t = (int64_t)c0 + b + i, d = (int64_t)c0 + i;
+    const bool has_q = i < g;
+    const int par = k & 1;
+
+    int x = -1;
+    float lx = 0.0f, qx = 0.0f;
+    bool valid = true;
+    if (tid == 0 && has_q) {
+      x = __ldg(P.ids + d);
+      valid = (x >= 0 && x < V);
+      if (valid) {
+        lx = load_logit(reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V + x);
+        qx = __ldg(P.q + d * (int64_t)V + x);
+      }
+    }
+
+    // ---- sweep 1 ------------------------------------------------------------
+    float m0 = -INFINITY, s0 = 0.0f;
+    for (int c = 0; c < n1; ++c, ++cc) {
+      const int s = cc % NS;
+      ok &= stream_wait(S, smem_addr(&S.full[s]), (cc / NS) & 1);
+      const int nvec = min(kEl1, V - c * kEl1) * (int)sizeof(TT) / 16;
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageBytes);
+      for (int j = tid; j < nvec; j += kStreamConsumers) softmax_acc16<TT>(st[j], m0, s0, P.c);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.empty[s]));
+    }
+    warp_softmax(m0, s0, P.c);
+    if (lane == 0) S.red[par][warp] = make_float4(m0, s0, 0.f, 0.f);
+    named_bar_sync(1, kStreamConsumers);
+    float M = -INFINITY, Ssum = 0.0f;
+    for (int w = 0; w < kStreamConsumerWarps; ++w) softmax_merge(M, Ssum, S.red[par][w].x, S.red[par][w].y, P.c);
+    const float invS = 1.0f / Ssum;
+
+    if (tid == 0) {
+      const int prefix = (i > 0 && prefix0 == kPrefixUnknown)
+                             ? read_prefix(P.status, t - i, i, P.epoch) : prefix0;
+      float px = 0.0f;
+      bool acc = false;
+      if (has_q) {
+        if (valid) px = ex2((lx - M) * P.c) * invS;
+        const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
+        acc = accept_test(r, px, qx);
+      }
+      const bool race = (prefix == kPrefixAllAccepted) && (!has_q || !acc);
+      S.dec[0] = px;
+      S.dec[1] = qx;
+      S.dec[2] = __int_as_float((acc ? 1 : 0) | (race ? 2 : 0) | (valid ? 0 : 4));
+    }
+    named_bar_sync(1, kStreamConsumers);
+    const int flags = __float_as_int(S.dec[2]);
+    const bool acc = flags & 1, race = flags & 2;
+    const bool resid = has_q && !acc;
+    const uint64_t rkey = stream_key(P.seed, P.req_offset + b, i, 1);
+
+    // ---- sweep 2: groups of one target stage and its draft stages ------------
+    float beta = 0.0f;
+    Race best = race_none();
+    for (int c = 0; c < n1; ++c) {
+      const int ne = min(kEl1, V - c * kEl1);
+      const int st_t = cc % NS;
+      ok &= stream_wait(S, smem_addr(&S.full[st_t]), (cc / NS) & 1);
+      ++cc;
+      int st_q[kQPerGroup];
+      int nqs = 0;
+      if (has_q) {
+        for (int h = 0; h < kQPerGroup; ++h)
+          if (c * kQPerGroup + h < nq) {
+            st_q[h] = cc % NS;
+            ok &= stream_wait(S, smem_addr(&S.full[st_q[h]]), (cc / NS) & 1);
+            ++cc;
+            ++nqs;
+          }
+      }
+      if (has_q || race) {
+        const unsigned char* tst = ring + (size_t)st_t * kStageBytes;
+        for (int e4 = tid; e4 * 4 < ne; e4 += kStreamConsumers) {
+          float l[4];
+          if constexpr (sizeof(TT) == 2) {
+            const uint2 w = reinterpret_cast<const uint2*>(tst)[e4];
+            l[0] = bf16_lo(w.x); l[1] = bf16_hi(w.x); l[2] = bf16_lo(w.y); l[3] = bf16_hi(w.y);
+          } else {
+            const float4 w = reinterpret_cast<const float4*>(tst)[e4];
+            l[0] = w.x; l[1] = w.y; l[2] = w.z; l[3] = w.w;
+          }
+          float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (has_q)
+            q4 = reinterpret_cast<const float4*>(ring + (size_t)st_q[e4 >> 10] * kStageBytes)[e4 & 1023];
+          const uint32_t v = (uint32_t)(c * kEl1 + 4 * e4);
+          if (has_q && race)
+            sweep2_4<true, true>(l, q4, M, P.c, invS, resid, rkey, v, beta, best);
+          else if (has_q)
+            sweep2_4<true, false>(l, q4, M, P.c, invS, resid, rkey, v, beta, best);
+          else
+            sweep2_4<false, true>(l, q4, M, P.c, invS, resid, rkey, v, beta, best);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&S.empty[st_t]));
+        for (int h = 0; h < nqs; ++h) mbar_arrive(smem_addr(&S.empty[st_q[h]]));
+      }
+    }
+    beta = warp_sum(beta);
+    warp_race(best);
+    if (lane == 0) S.red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
+    named_bar_sync(1, kStreamConsumers);
+    if (tid == 0) {
+      float bt = 0.0f;
+      Race tb = race_none();
+      for (int w = 0; w < kStreamConsumerWarps; ++w) {
+        const float4 r4 = S.red[par ^ 1][w];
+        bt += r4.x;
+        race_merge(tb, r4.y, r4.z, __float_as_int(r4.w));
+      }
+      if (ok) {
+        P.row_stats[t] = make_float2(M, Ssum);
+        uint32_t stw = kStDone;
+        if (has_q) {
+          if (flags & 4) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+          if (acc) stw |= kStAccepted;
+          if (P.out_beta) P.out_beta[d] = bt;
+          if (P.out_px) P.out_px[d] = S.dec[0];
+          if (P.out_qx) P.out_qx[d] = S.dec[1];
+          if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+        }
+        if (race && tb.w > 0.0f) {
+          P.out_tokens[t] = tb.idx;
+          stw |= kStRaceDone;
+        }
+        st_relaxed_u64(P.status + t, make_status(P.epoch, stw));
+      }
+      mbar_arrive(smem_addr(&S.dempty[ds]));
+    }
+    if (named_bar_or(1, kStreamConsumers, !ok)) {
+      if (tid == 0) set_err(P.err, SPECDEC_DEVERR_TIMEOUT);
+      break;
+    }
   }
 }
 
@@ -855,16 +1178,33 @@ static __global__ void finalize_kernel(const Params P) {
 }
 
 // ---------------------------------------------------------------------------
-// Race for deferred requests: one block per request, re-reads row (b, n_b)
-// (and the draft row when it is a correction).  Falls back to w = p when the
-// residual max(0, p - q) is zero everywhere (only reachable through rounding).
+// Race for deferred requests: re-reads row (b, n_b) (and the draft row when it
+// is a correction), split into slices over several CTAs.  Each CTA writes the
+// best candidate of its slice; the last CTA of a request (counted with an
+// atomic) merges them and writes the token.  When the residual max(0, p - q) is
+// zero everywhere (reachable only through rounding) that CTA races over p.
 // ---------------------------------------------------------------------------
+template <typename TT>
+__device__ __forceinline__ Race block_race(Race best, float4* red) {
+  warp_race(best);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0)
+    red[threadIdx.x >> 5] = make_float4(best.w, best.e, __int_as_float(best.idx), 0.f);
+  __syncthreads();
+  Race tb = race_none();
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) race_merge(tb, red[w].x, red[w].y, __float_as_int(red[w].z));
+  return tb;
+}
+
 template <typename TT>
 __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
   __shared__ float4 red[kRowThreads / 32];
+  __shared__ int s_last;
   const int V = P.V;
   const int count = *P.defer_count;
-  for (int k = blockIdx.x; k < count; k += gridDim.x) {
+  const int S = P.rslices;
+  for (int64_t item = blockIdx.x; item < (int64_t)count * S; item += gridDim.x) {
+    const int k = (int)(item / S), sl = (int)(item % S);
     const int b = P.defer_list[k];
     const int n = P.ws_nacc[b];
     const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
@@ -875,24 +1215,35 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
     const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
     const float* qrow = has_q ? P.q + ((int64_t)c0 + n) * (int64_t)V : nullptr;
     const uint64_t rkey = stream_key(P.seed, P.req_offset + b, n, 1);
-    for (int attempt = 0; attempt < 2; ++attempt) {
-      const bool resid = has_q && attempt == 0;
-      Race best = race_none();
-      for (int v = threadIdx.x; v < V; v += blockDim.x) {
-        const float p = ex2((load_logit(row + v) - ms.x) * P.c) * invS;
-        race_offer(best, resid ? fmaxf(p - __ldg(qrow + v), 0.0f) : p, rkey, (uint32_t)v);
+    const int v0 = sl * P.rslice_len, v1 = min(V, v0 + P.rslice_len);
+    Race best = race_none();
+    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+      const float p = ex2((load_logit(row + v) - ms.x) * P.c) * invS;
+      race_offer(best, has_q ? fmaxf(p - __ldg(qrow + v), 0.0f) : p, rkey, (uint32_t)v);
+    }
+    const Race tb = block_race<TT>(best, red);
+    if (threadIdx.x == 0) {
+      P.rpart[(int64_t)k * kRaceMaxSlices + sl] = make_float4(tb.w, tb.e, __int_as_float(tb.idx), 0.f);
+      __threadfence();
+      s_last = (atomicAdd(P.rcount + k, 1) == S - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      Race all = race_none();
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float4 r = __ldcg(P.rpart + (int64_t)k * kRaceMaxSlices + s2);
+        race_merge(all, r.x, r.y, __float_as_int(r.z));
       }
-      warp_race(best);
-      __syncthreads();
-      if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = make_float4(best.w, best.e, __int_as_float(best.idx), 0.f);
-      __syncthreads();
-      Race tb = race_none();
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
-        race_merge(tb, red[w].x, red[w].y, __float_as_int(red[w].z));
-      if (tb.w > 0.0f) {
-        if (threadIdx.x == 0) P.out_tokens[t] = tb.idx;
-        break;
+      if (!(all.w > 0.0f)) {  // empty residual: race over p instead
+        Race bp = race_none();
+        for (int v = threadIdx.x; v < V; v += blockDim.x)
+          race_offer(bp, ex2((load_logit(row + v) - ms.x) * P.c) * invS, rkey, (uint32_t)v);
+        all = block_race<TT>(bp, red);
+      }
+      if (threadIdx.x == 0) {
+        P.out_tokens[t] = all.idx;
+        P.rcount[k] = 0;
       }
     }
     __syncthreads();

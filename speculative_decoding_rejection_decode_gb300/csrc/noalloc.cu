@@ -25,18 +25,21 @@ namespace {
 constexpr int64_t kRows = SPECDEC_NOALLOC_MAX_ROWS;
 constexpr int kBatch = SPECDEC_NOALLOC_MAX_BATCH;
 constexpr int kParts = 16;  // greedy argmax slices per row, as in the handle path
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;  // sweep kernel: 2 CTAs of 512 threads per SM
 
 constexpr size_t kStatsOff = 0;
 constexpr size_t kStatusOff = kStatsOff + kRows * sizeof(float2);
 constexpr size_t kKeysOff = kStatusOff + kRows * sizeof(uint64_t);
 constexpr size_t kNaccOff = kKeysOff + kRows * kParts * sizeof(uint64_t);
 constexpr size_t kListOff = kNaccOff + kBatch * sizeof(int32_t);
-constexpr size_t kSmallOff = kListOff + kBatch * sizeof(int32_t);  // err, defer count, counter
+constexpr size_t kRpartOff = kListOff + kBatch * sizeof(int32_t);
+constexpr size_t kRcountOff = kRpartOff + (size_t)kBatch * kRaceMaxSlices * sizeof(float4);
+constexpr size_t kSmallOff = kRcountOff + kBatch * sizeof(int32_t);  // err, defer count, counter
 constexpr size_t kSmallBytes = 64;
 constexpr size_t kScratchBytes = kSmallOff + kSmallBytes;
 static_assert(kStatusOff % 256 == 0 && kKeysOff % 256 == 0 && kNaccOff % 256 == 0 &&
-                  kListOff % 256 == 0 && kSmallOff % 256 == 0,
+                  kListOff % 256 == 0 && kRpartOff % 256 == 0 && kRcountOff % 256 == 0 &&
+                  kSmallOff % 256 == 0,
               "scratch sections stay 256-byte aligned");
 
 }  // namespace
@@ -116,6 +119,10 @@ extern "C" int specdec_rejection_sample_noalloc(
   P.gkeys = reinterpret_cast<uint64_t*>(base + kKeysOff);
   P.ws_nacc = reinterpret_cast<int32_t*>(base + kNaccOff);
   P.defer_list = reinterpret_cast<int32_t*>(base + kListOff);
+  P.rpart = reinterpret_cast<float4*>(base + kRpartOff);
+  P.rcount = reinterpret_cast<int32_t*>(base + kRcountOff);
+  P.rslices = (int)std::min<int64_t>(kRaceMaxSlices, std::max<int64_t>(1, (V + 4095) / 4096));
+  P.rslice_len = (int)(((V + P.rslices - 1) / P.rslices + 7) / 8 * 8);
   P.err = out_device_error ? out_device_error : small;
   P.defer_count = reinterpret_cast<int32_t*>(small + 1);
   P.sched = reinterpret_cast<unsigned long long*>(small + 2);
@@ -140,13 +147,13 @@ extern "C" int specdec_rejection_sample_noalloc(
     P.vec_ok = ((int64_t)V * esize) % 16 == 0 && ((int64_t)V * 4) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
-    const int race_grid = std::max(1, std::min(B, sms * 4));
+    const int race_grid = sms * 4;
     if (dtype == SPECDEC_BF16) {
-      sweep_row_kernel<__nv_bfloat16, kThreads><<<sms, kThreads, 0, st>>>(P);
+      sweep_row_kernel<__nv_bfloat16, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
       finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
       race_kernel<__nv_bfloat16><<<race_grid, kRowThreads, 0, st>>>(P);
     } else {
-      sweep_row_kernel<float, kThreads><<<sms, kThreads, 0, st>>>(P);
+      sweep_row_kernel<float, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
       finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
       race_kernel<float><<<race_grid, kRowThreads, 0, st>>>(P);
     }

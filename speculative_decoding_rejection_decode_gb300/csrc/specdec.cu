@@ -17,7 +17,6 @@ namespace {
 constexpr int kGreedyMaxParts = 16;
 constexpr int kClusterSizes[5] = {1, 2, 4, 8, 16};
 constexpr int kMinRing = 3;  // draft ring stages the fused kernel needs at least
-constexpr int kSweepThreads = 1024;
 
 struct Workspace {
   void* base = nullptr;
@@ -28,6 +27,8 @@ struct Workspace {
   uint64_t* gkeys = nullptr;
   int32_t* ws_nacc = nullptr;
   int32_t* defer_list = nullptr;
+  float4* rpart = nullptr;
+  int32_t* rcount = nullptr;
 };
 
 struct FusedConfig {
@@ -51,6 +52,10 @@ struct specdec_ctx {
   int path_override = SPECDEC_PATH_AUTO;
   int last_path = 0, last_cluster = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+  int stream_smem[4] = {0, 0, 0, 0};  // dynamic shared memory set on stream_row_kernel<dtype, ctas>
+  int smem_per_sm = 0;
+  int sweep_threads = 512;      // block size of the sweep kernel (1024 x 1, 512 x 2, 256 x 4 per SM)
+  int stream_ctas = 1;          // stream kernel CTAs per SM (1 or 2)
   int occ_cache[2][5][2] = {};  // [dtype][cluster index] -> {smem, clusters}
 };
 
@@ -74,7 +79,9 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   const size_t gkeys_b = round_up(rows * kGreedyMaxParts * sizeof(uint64_t), 256);
   const size_t nacc_b = round_up((size_t)b * sizeof(int32_t), 256);
   const size_t list_b = nacc_b;
-  const size_t total = stats_b + status_b + gkeys_b + nacc_b + list_b;
+  const size_t rpart_b = round_up((size_t)b * kRaceMaxSlices * sizeof(float4), 256);
+  const size_t rcount_b = nacc_b;
+  const size_t total = stats_b + status_b + gkeys_b + nacc_b + list_b + rpart_b + rcount_b;
   if (cudaDeviceSynchronize() != cudaSuccess) return SPECDEC_ERR_CUDA;
   free_workspace(h);
   void* p = nullptr;
@@ -94,6 +101,10 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   h->ws.ws_nacc = reinterpret_cast<int32_t*>(c);
   c += nacc_b;
   h->ws.defer_list = reinterpret_cast<int32_t*>(c);
+  c += list_b;
+  h->ws.rpart = reinterpret_cast<float4*>(c);
+  c += rpart_b;
+  h->ws.rcount = reinterpret_cast<int32_t*>(c);
   h->ws.cap_rows = rows;
   h->ws.cap_b = b;
   return SPECDEC_OK;
@@ -176,8 +187,28 @@ template <typename TT>
 int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, cudaStream_t st) {
   const int B = P.B;
   if (h->ev_before) cudaEventRecord(h->ev_before, st);
-  if (path == SPECDEC_PATH_SWEEP) {
-    sweep_row_kernel<TT, kSweepThreads><<<h->num_sms, kSweepThreads, 0, st>>>(P);
+  if (path == SPECDEC_PATH_STREAM) {
+    const int ctas = h->stream_ctas;
+    const int fixed = (int)((sizeof(StreamShared) + 127) / 128 * 128);
+    const int budget = ctas == 1 ? h->smem_optin : h->smem_per_sm / 2 - 1024;
+    const int ns = std::min(kMaxStages, (budget - fixed) / kStageBytes);
+    const int smem = ns * kStageBytes + fixed;
+    P.nq = ns;
+    auto kern = ctas == 1 ? stream_row_kernel<TT, 1> : stream_row_kernel<TT, 2>;
+    int& cached = h->stream_smem[(sizeof(TT) == 2) * 2 + (ctas - 1)];
+    if (cached != smem) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return SPECDEC_ERR_CUDA;
+      cached = smem;
+    }
+    kern<<<h->num_sms * ctas, kStreamThreads, smem, st>>>(P);
+  } else if (path == SPECDEC_PATH_SWEEP) {
+    if (h->sweep_threads == 512)
+      sweep_row_kernel<TT, 512, 2><<<h->num_sms * 2, 512, 0, st>>>(P);
+    else if (h->sweep_threads == 256)
+      sweep_row_kernel<TT, 256, 4><<<h->num_sms * 4, 256, 0, st>>>(P);
+    else
+      sweep_row_kernel<TT, 1024, 1><<<h->num_sms, 1024, 0, st>>>(P);
   } else if (path == SPECDEC_PATH_FUSED) {
     P.slice_len = f.slice_len;
     P.tbuf_bytes = f.tbuf_bytes;
@@ -202,7 +233,7 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
   }
   if (h->ev_after) cudaEventRecord(h->ev_after, st);
   finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
-  race_kernel<TT><<<std::max(1, std::min(B, h->num_sms * 4)), kRowThreads, 0, st>>>(P);
+  race_kernel<TT><<<h->num_sms * 4, kRowThreads, 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
@@ -240,6 +271,16 @@ int specdec_create(specdec_handle_t* out, int device) {
   h->device = device;
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  cudaDeviceGetAttribute(&h->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
+  // tuning knobs for measurements: sweep block size (1024, 512, 256) and stream CTAs per SM
+  if (const char* e = std::getenv("SPECDEC_SWEEP_THREADS")) {
+    const int v = std::atoi(e);
+    if (v == 256 || v == 512 || v == 1024) h->sweep_threads = v;
+  }
+  if (const char* e = std::getenv("SPECDEC_STREAM_CTAS")) {
+    const int v = std::atoi(e);
+    if (v == 1 || v == 2) h->stream_ctas = v;
+  }
   if (cudaMalloc(&h->small, 64) != cudaSuccess || cudaMemset(h->small, 0, 64) != cudaSuccess) {
     delete h;
     return SPECDEC_ERR_OOM;
@@ -299,6 +340,10 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
   P.gkeys = h->ws.gkeys;
   P.ws_nacc = h->ws.ws_nacc;
   P.defer_list = h->ws.defer_list;
+  P.rpart = h->ws.rpart;
+  P.rcount = h->ws.rcount;
+  P.rslices = (int)std::min<int64_t>(kRaceMaxSlices, std::max<int64_t>(1, (V + 4095) / 4096));
+  P.rslice_len = (int)round_up((V + P.rslices - 1) / P.rslices, 8);
   P.defer_count = reinterpret_cast<int32_t*>(h->small + 1);
   P.err = h->small;
   P.cap_rows = h->ws.cap_rows;
@@ -319,6 +364,7 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
              reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
   P.sched = reinterpret_cast<unsigned long long*>(h->small + 2);
   int path = h->path_override == SPECDEC_PATH_AUTO ? SPECDEC_PATH_SWEEP : h->path_override;
+  if (path == SPECDEC_PATH_STREAM && !P.vec_ok) path = SPECDEC_PATH_SWEEP;
   FusedConfig f;
   if (path == SPECDEC_PATH_FUSED) {
     f = dtype == SPECDEC_BF16 ? fused_config<__nv_bfloat16>(h, dtype, V, target_logits, draft_probs)
@@ -355,7 +401,8 @@ int specdec_get_error(specdec_handle_t h, int* device_error, void* stream) {
 }
 
 int specdec_set_path(specdec_handle_t h, int path) {
-  if (!h || path < SPECDEC_PATH_AUTO || path > SPECDEC_PATH_SWEEP) return SPECDEC_ERR_INVALID_ARG;
+  if (!h || path < SPECDEC_PATH_AUTO || path > SPECDEC_PATH_STREAM || path == SPECDEC_PATH_GREEDY)
+    return SPECDEC_ERR_INVALID_ARG;
   h->path_override = path;
   return SPECDEC_OK;
 }

@@ -30,12 +30,13 @@ def V():
 
 
 def _paths():
-    from speculative_decoding_rejection_decode_gb300 import (SPECDEC_PATH_FUSED, SPECDEC_PATH_SWEEP,
-                                                             SPECDEC_PATH_TWO_PASS)
-    return {"fused": SPECDEC_PATH_FUSED, "sweep": SPECDEC_PATH_SWEEP, "two_pass": SPECDEC_PATH_TWO_PASS}
+    from speculative_decoding_rejection_decode_gb300 import (SPECDEC_PATH_FUSED, SPECDEC_PATH_STREAM,
+                                                             SPECDEC_PATH_SWEEP, SPECDEC_PATH_TWO_PASS)
+    return {"fused": SPECDEC_PATH_FUSED, "sweep": SPECDEC_PATH_SWEEP, "stream": SPECDEC_PATH_STREAM,
+            "two_pass": SPECDEC_PATH_TWO_PASS}
 
 
-ALL_PATHS = ["fused", "sweep", "two_pass"]
+ALL_PATHS = ["stream", "fused", "sweep", "two_pass"]
 
 
 # --------------------------------------------------------------------------
@@ -128,7 +129,7 @@ def test_config4_full_size_sampled(V):
     w = make_config(4, device="cuda")
     g = run_gpu(V, w)
     assert V.get_error() == 0
-    assert V.last_path()[0] in (_paths()["fused"], _paths()["sweep"])
+    assert V.last_path()[0] == _paths()["sweep"]
     cu = w.cu.cpu().numpy()
     # properties that hold for every request
     sc.check_e_layout(g["tokens"], g["num_accepted"], w.draft_ids.cpu().numpy(), cu, w.V)
