@@ -494,6 +494,8 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
                                        float M, float c, float invS, bool resid, uint64_t rkey,
                                        uint64_t pol, float& beta, Race& best) {
   constexpr int kEl = 16 / sizeof(TT);
+  // target vectors loaded per iteration: fewer where the race needs registers
+  constexpr int U = kRace ? 2 : (sizeof(TT) == 2 ? 3 : 4);
   const int tid = threadIdx.x;
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (vec) {
@@ -501,11 +503,11 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
     const uint4* qv = reinterpret_cast<const uint4*>(qrow);
     const int nv = V / kEl;
     int j = tid;
-    for (; j + NT < nv; j += 2 * NT) {
-      uint4 a[2];
-      uint4 b[2][kEl / 4];
+    for (; j + (U - 1) * NT < nv; j += U * NT) {
+      uint4 a[U];
+      uint4 b[U][kEl / 4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
         a[u] = ldg_hint(rv + j + u * NT, pol);
         if constexpr (kHasQ) {
 #pragma unroll
@@ -513,7 +515,7 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
         float x[kEl];
         unpack16<TT>(a[u], x);
 #pragma unroll
@@ -641,13 +643,15 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
       const uint4* rv = reinterpret_cast<const uint4*>(row);
       const int nv = V / kEl;
       int j = tid;
-      for (; j + 3 * NT < nv; j += 4 * NT) {
-        const uint4 a0 = ldg_hint(rv + j, keep), a1 = ldg_hint(rv + j + NT, keep);
-        const uint4 a2 = ldg_hint(rv + j + 2 * NT, keep), a3 = ldg_hint(rv + j + 3 * NT, keep);
-        softmax_acc16<TT>(a0, m0, s0, P.c);
-        softmax_acc16<TT>(a1, m1, s1, P.c);
-        softmax_acc16<TT>(a2, m0, s0, P.c);
-        softmax_acc16<TT>(a3, m1, s1, P.c);
+      for (; j + 7 * NT < nv; j += 8 * NT) {   // 8 vectors (128 B) in flight per thread
+        uint4 a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a[u] = ldg_hint(rv + j + u * NT, keep);
+#pragma unroll
+        for (int u = 0; u < 8; u += 2) {
+          softmax_acc16<TT>(a[u], m0, s0, P.c);
+          softmax_acc16<TT>(a[u + 1], m1, s1, P.c);
+        }
       }
       for (; j < nv; j += NT) softmax_acc16<TT>(ldg_hint(rv + j, keep), m0, s0, P.c);
     } else {
