@@ -188,7 +188,7 @@ int specdec_neg_log_uniform(uint32_t k0, int64_t n, float* out, void* stream);
  * pre-allocated buffers, hosts that freeze device allocation after start-up).
  * It needs no handle and allocates nothing: its scratch (per-row softmax
  * statistics and status words, the deferred-request list, a few counters) is
- * one file-scope device array of about 3.5 MB, which every GPU that loads the
+ * one file-scope device array of about 1.5 MB, which every GPU that loads the
  * library holds until the process exits.  It runs the same kernels as
  * specdec_rejection_sample (the sweep path for T > 0, the greedy path at
  * T == 0) with the same arguments, plus:

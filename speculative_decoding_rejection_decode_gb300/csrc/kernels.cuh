@@ -14,7 +14,8 @@
 //   race_kernel        the race for requests whose extra token the row kernel could
 //                      not draw (its row ran before the earlier rows of the request
 //                      finished): re-reads that single row.
-//   greedy_*           T = 0: argmax partials per row slice, then the scan.
+//   greedy_*           T = 0: argmax per row (warp items, 64-bit atomicMax), then
+//                      the scan.
 //
 // Method: Algorithm 1 and Section 2.3 of Leviathan et al. as restated on the
 // bloss0m and vllbc reading-notes pages; accept test r < min(1, p/q) as in the
@@ -51,7 +52,7 @@ struct Params {
   // workspace
   float2* row_stats;       // [cap_rows] (max, sum) of each target row
   uint64_t* status;        // [cap_rows]
-  uint64_t* gkeys;         // [cap_rows * gparts] greedy partial argmax keys
+  uint64_t* gkeys;         // [cap_rows] greedy argmax key per row (0 between calls)
   int32_t* ws_nacc;        // [cap_B] n_b for the race kernel
   int32_t* defer_list;     // [cap_B]
   int32_t* defer_count;    // [1]
@@ -63,8 +64,6 @@ struct Params {
   uint32_t* err;           // [1] sticky device error word
   int64_t cap_rows;
   int cap_b;
-  int gparts;              // greedy: slices per row
-  int gpart_len;           // greedy: elements per slice (multiple of 8)
   // fused kernel geometry
   int slice_len;           // elements per cluster rank (multiple of 8)
   int tbuf_bytes;          // bytes of the target slice buffer (rank 0, 128-aligned)
@@ -1257,96 +1256,127 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
 // ---------------------------------------------------------------------------
 // Greedy path (T == 0).
 // ---------------------------------------------------------------------------
+// Argmax of every target row.  Work items are (row, chunk) pairs, a chunk being
+// 256 vectors of 16 bytes (or 256 elements when rows are not 16-byte aligned);
+// each warp takes items in grid-stride order, keeps 8 loads per lane in flight,
+// reduces the packed (value, -index) keys over the warp and folds its result
+// into the row's key with one 64-bit atomicMax.  No block-level barrier.  The
+// finalize kernel reads the row keys and resets them to 0 for the next call.
 template <typename TT>
 __global__ void __launch_bounds__(kRowThreads) greedy_partial_kernel(const Params P, int vec_ok) {
-  __shared__ uint64_t red[kRowThreads / 32];
-  const int B = P.B, V = P.V, parts = P.gparts, plen = P.gpart_len;
+  constexpr int kEl = 16 / sizeof(TT);
+  constexpr int kPer = 8;                 // loads per lane per item
+  constexpr int kChunkVec = 32 * kPer;    // vectors (or elements) per item
+  const int B = P.B, V = P.V;
   const int64_t n_t = min((int64_t)__ldg(P.cu + B) + B, P.cap_rows);
   if (blockIdx.x == 0 && threadIdx.x == 0 && (int64_t)__ldg(P.cu + B) + B > P.cap_rows)
     set_err(P.err, SPECDEC_DEVERR_CAPACITY);
-  const int64_t units = n_t * parts;
-  constexpr int kEl = 16 / sizeof(TT);
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int64_t t = u / parts;
-    const int part = (int)(u % parts);
-    const int v0 = part * plen, v1 = min(V, v0 + plen);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int per_row = vec_ok ? (V / kEl + kChunkVec - 1) / kChunkVec : (V + kChunkVec - 1) / kChunkVec;
+  const int64_t items = n_t * per_row;
+  for (int64_t it = warp_id; it < items; it += nwarps) {
+    const int64_t t = it / per_row;
+    const int ch = (int)(it % per_row);
+    // only rows of well-formed requests are accumulated: exactly the rows the
+    // finalize kernel reads and resets
+    const int b = request_of_target(P.cu, B, t);
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t0 = (int64_t)c0 + b;
+    if (g < 0 || t < t0 || t > t0 + g || t0 + g >= P.cap_rows) continue;
     const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
-    uint64_t best = 0;
+    // Each lane scans its elements in increasing index order, so a strict
+    // "greater" keeps the lowest index on ties (and -0.0 == +0.0, as numbers).
+    float bv = -INFINITY;
+    int bi = -1;
     if (vec_ok) {
-      for (int e = v0 + threadIdx.x * kEl; e < v1; e += blockDim.x * kEl) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + e));
-        if constexpr (sizeof(TT) == 2) {
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      const int nv = V / kEl;
+      const int j0 = ch * kChunkVec + lane;
+      uint4 w[kPer];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint64_t a = argmax_key(bf16_lo(ws[k]), e + 2 * k);
-            uint64_t c = argmax_key(bf16_hi(ws[k]), e + 2 * k + 1);
-            best = a > best ? a : best;
-            best = c > best ? c : best;
+      for (int k = 0; k < kPer; ++k)
+        if (j0 + 32 * k < nv) w[k] = __ldg(reinterpret_cast<const uint4*>(row) + j0 + 32 * k);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int j = j0 + 32 * k;
+        if (j >= nv) break;
+        float x[kEl];
+        unpack16<TT>(w[k], x);
+#pragma unroll
+        for (int h = 0; h < kEl; ++h)
+          if (x[h] > bv || bi < 0) {
+            bv = x[h];
+            bi = j * kEl + h;
           }
-        } else {
-          const float f[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                              __uint_as_float(w.w)};
+      }
+    } else {
+      const int v0 = ch * kChunkVec + lane;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint64_t a = argmax_key(f[k], e + k);
-            best = a > best ? a : best;
+      for (int k = 0; k < kPer; ++k) {
+        const int v = v0 + 32 * k;
+        if (v < V) {
+          const float x = load_logit(row + v);
+          if (x > bv || bi < 0) {
+            bv = x;
+            bi = v;
           }
         }
       }
-    } else {
-      for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-        uint64_t a = argmax_key(load_logit(row + v), v);
-        best = a > best ? a : best;
-      }
     }
+    uint64_t best = bi < 0 ? 0ull : argmax_key(bv, (uint32_t)bi);
     best = warp_max_u64(best);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint64_t bt = 0;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) bt = red[w] > bt ? red[w] : bt;
-      P.gkeys[u] = bt;
-    }
+    if (lane == 0) atomicMax(reinterpret_cast<unsigned long long*>(P.gkeys + t), (unsigned long long)best);
   }
 }
 
+// One warp per request: lanes combine the partial argmax keys of the request's
+// rows (lowest index on ties is built into the keys), lane 0 scans.
 static __global__ void greedy_finalize_kernel(const Params P) {
-  const int B = P.B, V = P.V, parts = P.gparts;
-  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+  __shared__ int s_g[8][33];
+  const int B = P.B, V = P.V;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  for (int b = blockIdx.x * 8 + wib; b < B; b += gridDim.x * 8) {
     const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
     const int64_t t0 = (int64_t)c0 + b;
     if (g < 0 || t0 + g >= P.cap_rows) continue;
     int n = g, tok = -1;
-    for (int i = 0; i <= g; ++i) {
-      uint64_t k = 0;
-      for (int p = 0; p < parts; ++p) {
-        const uint64_t a = P.gkeys[(t0 + i) * parts + p];
-        k = a > k ? a : k;
+    bool found = false;
+    // rows in chunks of 32 (row = chunk base + lane); every position's outputs
+    // are written, also after the first rejection
+    for (int i0 = 0; i0 <= g; i0 += 32) {
+      const int i = i0 + lane;
+      int gi = -1;
+      if (i <= g) {
+        gi = (int)argmax_key_index(P.gkeys[t0 + i]);
+        P.gkeys[t0 + i] = 0;  // ready for the next call
       }
-      const int gi = (int)argmax_key_index(k);
-      if (i == g) {
-        if (n == g) tok = gi;
-        break;
+      s_g[wib][lane] = gi;
+      int acc = 0;
+      if (i < g) {
+        const int x = __ldg(P.ids + c0 + i);
+        if (x < 0 || x >= V) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+        acc = (x == gi);
+        const int64_t d = (int64_t)c0 + i;
+        if (P.out_beta) P.out_beta[d] = acc ? 1.0f : 0.0f;
+        if (P.out_px) P.out_px[d] = acc ? 1.0f : 0.0f;
+        if (P.out_qx) P.out_qx[d] = 1.0f;
+        if (P.out_acc) P.out_acc[d] = acc;
       }
-      const int x = __ldg(P.ids + c0 + i);
-      if (x < 0 || x >= V) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
-      const bool acc = (x == gi);
-      const int64_t d = (int64_t)c0 + i;
-      if (P.out_beta) P.out_beta[d] = acc ? 1.0f : 0.0f;
-      if (P.out_px) P.out_px[d] = acc ? 1.0f : 0.0f;
-      if (P.out_qx) P.out_qx[d] = 1.0f;
-      if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
-      if (!acc && n == g) {
-        n = i;
-        tok = gi;
+      __syncwarp();
+      // first rejected draft in this chunk (the bonus slot i == g counts as the stop)
+      const unsigned stop = __ballot_sync(0xFFFFFFFFu, (i < g && !acc) || i == g);
+      if (stop && !found) {
+        const int f = __ffs(stop) - 1;
+        n = i0 + f;
+        tok = s_g[wib][f];
+        found = true;
       }
+      __syncwarp();
     }
-    P.out_nacc[b] = n;
-    for (int i = 0; i < n; ++i) P.out_tokens[t0 + i] = __ldg(P.ids + c0 + i);
-    P.out_tokens[t0 + n] = tok;
-    for (int i = n + 1; i <= g; ++i) P.out_tokens[t0 + i] = -1;
+    if (lane == 0) P.out_nacc[b] = n;
+    for (int i = lane; i <= g; i += 32)
+      P.out_tokens[t0 + i] = i < n ? __ldg(P.ids + c0 + i) : (i == n ? tok : -1);
   }
 }
 

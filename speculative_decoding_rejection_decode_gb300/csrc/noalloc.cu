@@ -24,13 +24,12 @@ namespace {
 
 constexpr int64_t kRows = SPECDEC_NOALLOC_MAX_ROWS;
 constexpr int kBatch = SPECDEC_NOALLOC_MAX_BATCH;
-constexpr int kParts = 16;  // greedy argmax slices per row, as in the handle path
 constexpr int kThreads = 512;  // sweep kernel: 2 CTAs of 512 threads per SM
 
 constexpr size_t kStatsOff = 0;
 constexpr size_t kStatusOff = kStatsOff + kRows * sizeof(float2);
 constexpr size_t kKeysOff = kStatusOff + kRows * sizeof(uint64_t);
-constexpr size_t kNaccOff = kKeysOff + kRows * kParts * sizeof(uint64_t);
+constexpr size_t kNaccOff = kKeysOff + kRows * sizeof(uint64_t);
 constexpr size_t kListOff = kNaccOff + kBatch * sizeof(int32_t);
 constexpr size_t kRpartOff = kListOff + kBatch * sizeof(int32_t);
 constexpr size_t kRcountOff = kRpartOff + (size_t)kBatch * kRaceMaxSlices * sizeof(float4);
@@ -131,18 +130,13 @@ extern "C" int specdec_rejection_sample_noalloc(
 
   const int esize = dtype == SPECDEC_BF16 ? 2 : 4;
   if (T == 0.0f) {
-    int parts = (int)std::min<int64_t>(kParts, std::max<int64_t>(1, (V + 16383) / 16384));
-    const int plen = (int)(((V + parts - 1) / parts + 7) / 8 * 8);
-    parts = (V + plen - 1) / plen;
-    P.gparts = parts;
-    P.gpart_len = plen;
     const int vec_ok = ((int64_t)V * esize) % 16 == 0 &&
                        reinterpret_cast<uintptr_t>(target_logits) % 16 == 0;
     if (dtype == SPECDEC_BF16)
       greedy_partial_kernel<__nv_bfloat16><<<sms * 8, kRowThreads, 0, st>>>(P, vec_ok);
     else
       greedy_partial_kernel<float><<<sms * 8, kRowThreads, 0, st>>>(P, vec_ok);
-    greedy_finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
+    greedy_finalize_kernel<<<(B + 7) / 8, 256, 0, st>>>(P);
   } else {
     P.vec_ok = ((int64_t)V * esize) % 16 == 0 && ((int64_t)V * 4) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&

@@ -14,7 +14,6 @@ using namespace specdec;
 
 namespace {
 
-constexpr int kGreedyMaxParts = 16;
 constexpr int kClusterSizes[5] = {1, 2, 4, 8, 16};
 constexpr int kMinRing = 3;  // draft ring stages the fused kernel needs at least
 
@@ -76,7 +75,7 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   b = std::max(b, 1);
   const size_t stats_b = round_up(rows * sizeof(float2), 256);
   const size_t status_b = round_up(rows * sizeof(uint64_t), 256);
-  const size_t gkeys_b = round_up(rows * kGreedyMaxParts * sizeof(uint64_t), 256);
+  const size_t gkeys_b = round_up(rows * sizeof(uint64_t), 256);
   const size_t nacc_b = round_up((size_t)b * sizeof(int32_t), 256);
   const size_t list_b = nacc_b;
   const size_t rpart_b = round_up((size_t)b * kRaceMaxSlices * sizeof(float4), 256);
@@ -239,16 +238,10 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
 
 template <typename TT>
 int launch_greedy(specdec_ctx* h, Params& P, bool vec_ok, cudaStream_t st) {
-  const int V = P.V;
-  int parts = (int)std::min<int64_t>(kGreedyMaxParts, std::max<int64_t>(1, (V + 16383) / 16384));
-  const int plen = (int)round_up((V + parts - 1) / parts, 8);
-  parts = (V + plen - 1) / plen;
-  P.gparts = parts;
-  P.gpart_len = plen;
   if (h->ev_before) cudaEventRecord(h->ev_before, st);
   greedy_partial_kernel<TT><<<h->num_sms * 8, kRowThreads, 0, st>>>(P, vec_ok ? 1 : 0);
   if (h->ev_after) cudaEventRecord(h->ev_after, st);
-  greedy_finalize_kernel<<<(P.B + 255) / 256, 256, 0, st>>>(P);
+  greedy_finalize_kernel<<<(P.B + 7) / 8, 256, 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 

@@ -288,6 +288,14 @@ def test_bf16_greedy_ties_and_signed_zero(V):
     compare(w, g, r, exact=True)
 
 
+def test_greedy_long_drafts(V):
+    # more than 32 drafts per request: the finalize scan runs over several chunks
+    w = make_workload(name="long", B=5, gamma=(0, 70), V=999, dtype="bf16", T=0.0, seed=41,
+                      ids="argmax0.75", device="cuda")
+    g = run_gpu(V, w)
+    compare(w, g, run_oracle(w), exact=True)
+
+
 def test_greedy_unaligned_vocab(V):
     w = make_config(2, B=10, V=1001)
     g = run_gpu(V, w)
