@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--config", type=int, default=4, help="standard workload 0..4")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V")
-    ap.add_argument("--path", choices=["auto", "fused", "sweep", "stream", "two_pass"], default="auto")
+    ap.add_argument("--path", choices=["auto", "fused", "sweep", "stream", "pair", "two_pass"],
+                    default="auto")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -254,7 +255,8 @@ def main():
     v.reserve(w.n_draft, w.B)
     if args.path != "auto":
         v.set_path({"fused": sd.SPECDEC_PATH_FUSED, "sweep": sd.SPECDEC_PATH_SWEEP,
-                    "stream": sd.SPECDEC_PATH_STREAM, "two_pass": sd.SPECDEC_PATH_TWO_PASS}[args.path])
+                    "stream": sd.SPECDEC_PATH_STREAM, "pair": sd.SPECDEC_PATH_PAIR,
+                    "two_pass": sd.SPECDEC_PATH_TWO_PASS}[args.path])
     out = sd.VerifyOutput(tokens=torch.empty(w.n_target, dtype=torch.int32, device=dev),
                           num_accepted=torch.empty(w.B, dtype=torch.int32, device=dev),
                           beta=torch.empty(w.n_draft, dtype=torch.float32, device=dev))
@@ -274,13 +276,13 @@ def main():
         raise RuntimeError("device error word set during warm-up")
     path, csize = v.last_path()
     launches_per_step = {sd.SPECDEC_PATH_FUSED: 3, sd.SPECDEC_PATH_TWO_PASS: 4,
-                         sd.SPECDEC_PATH_SWEEP: 3, sd.SPECDEC_PATH_STREAM: 3,
+                         sd.SPECDEC_PATH_SWEEP: 3, sd.SPECDEC_PATH_STREAM: 3, sd.SPECDEC_PATH_PAIR: 3,
                          sd.SPECDEC_PATH_GREEDY: 2}[path]
     kernel_name = {sd.SPECDEC_PATH_FUSED: "fused_row_kernel", sd.SPECDEC_PATH_SWEEP: "sweep_row_kernel",
-                   sd.SPECDEC_PATH_STREAM: "stream_row_kernel",
+                   sd.SPECDEC_PATH_STREAM: "stream_row_kernel", sd.SPECDEC_PATH_PAIR: "pair_row_kernel",
                    sd.SPECDEC_PATH_TWO_PASS: "stats_kernel+verify_kernel",
                    sd.SPECDEC_PATH_GREEDY: "greedy_partial_kernel"}[path]
-    path_name = {1: "fused", 2: "two_pass", 3: "sweep", 4: "greedy", 5: "stream"}[path]
+    path_name = {1: "fused", 2: "two_pass", 3: "sweep", 4: "greedy", 5: "stream", 6: "pair"}[path]
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),

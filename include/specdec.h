@@ -92,6 +92,8 @@ typedef struct specdec_ctx* specdec_handle_t;
 #define SPECDEC_PATH_GREEDY 4   /* reported by specdec_last_path for T == 0          */
 #define SPECDEC_PATH_STREAM 5   /* the two sweeps fed by bulk copies through a shared-
                                    memory ring (T > 0; needs 16-byte aligned rows)   */
+#define SPECDEC_PATH_PAIR 6     /* the two sweeps with each row split over a 2-CTA
+                                   cluster (T > 0)                                    */
 
 /* Creates a handle bound to CUDA device `device`.  *out receives the handle.
  * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (null out, bad device) or
@@ -155,7 +157,7 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream);
 
 /* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
- * _STREAM or _AUTO, the default, which takes SWEEP).  A forced FUSED or STREAM
+ * _STREAM, _PAIR or _AUTO, the default, which takes SWEEP).  A forced FUSED or STREAM
  * path falls back to SWEEP where its layout rules (16-byte aligned rows; for
  * FUSED a vocabulary that fits a cluster) do not hold. */
 int specdec_set_path(specdec_handle_t h, int path);
@@ -167,7 +169,7 @@ int specdec_set_path(specdec_handle_t h, int path);
 int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after_rows);
 
 /* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
- * _STREAM or _GREEDY), and the cluster size of the fused path (0 otherwise). */
+ * _STREAM, _PAIR or _GREEDY), and the cluster size of a cluster path (0 otherwise). */
 int specdec_last_path(specdec_handle_t h, int* path, int* cluster_size);
 
 /* Writes out[j] = U(seed, b, pos, stream_id, v0 + j) for j < n into device

@@ -38,6 +38,7 @@ SPECDEC_PATH_TWO_PASS = 2
 SPECDEC_PATH_SWEEP = 3
 SPECDEC_PATH_GREEDY = 4
 SPECDEC_PATH_STREAM = 5
+SPECDEC_PATH_PAIR = 6
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

@@ -488,8 +488,10 @@ __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float
   }
 }
 
+// Sweep 2 over vectors [lo, hi) of the row (elements [lo, hi) when the row is
+// not 16-byte aligned).
 template <typename TT, int NT, bool kHasQ, bool kRace>
-__device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, bool vec,
+__device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo, int hi, bool vec,
                                        float M, float c, float invS, bool resid, uint64_t rkey,
                                        uint64_t pol, float& beta, Race& best) {
   constexpr int kEl = 16 / sizeof(TT);
@@ -500,8 +502,8 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
   if (vec) {
     const uint4* rv = reinterpret_cast<const uint4*>(row);
     const uint4* qv = reinterpret_cast<const uint4*>(qrow);
-    const int nv = V / kEl;
-    int j = tid;
+    const int nv = hi;
+    int j = lo + tid;
     for (; j + (U - 1) * NT < nv; j += U * NT) {
       uint4 a[U];
       uint4 b[U][kEl / 4];
@@ -541,7 +543,7 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
       }
     }
   } else {
-    for (int v = tid; v < V; v += NT) {
+    for (int v = lo + tid; v < hi; v += NT) {
       const float p = ex2((load_logit(row + v) - M) * c) * invS;
       float qv = 0.0f;
       if constexpr (kHasQ) {
@@ -551,6 +553,42 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int V, 
       if constexpr (kRace) race_offer(best, (kHasQ && resid) ? fmaxf(p - qv, 0.0f) : p, rkey, (uint32_t)v);
     }
   }
+}
+
+// Sweep 1 over vectors [lo, hi) (elements when not aligned): per-thread online
+// (max, sum) in two interleaved accumulators, merged on return.
+template <typename TT, int NT>
+__device__ __forceinline__ void sweep1(const TT* row, int lo, int hi, bool vec, float c,
+                                       uint64_t pol, float& m, float& s) {
+  float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+  const int tid = threadIdx.x;
+  if (vec) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    int j = lo + tid;
+    for (; j + 7 * NT < hi; j += 8 * NT) {   // 8 vectors (128 B) in flight per thread
+      uint4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = ldg_hint(rv + j + u * NT, pol);
+#pragma unroll
+      for (int u = 0; u < 8; u += 2) {
+        softmax_acc16<TT>(a[u], m0, s0, c);
+        softmax_acc16<TT>(a[u + 1], m1, s1, c);
+      }
+    }
+    for (; j < hi; j += NT) softmax_acc16<TT>(ldg_hint(rv + j, pol), m0, s0, c);
+  } else {
+    for (int v = lo + tid; v < hi; v += NT) {
+      const float xv = load_logit(row + v);
+      if (xv > m0) {
+        s0 *= ex2((m0 - xv) * c);
+        m0 = xv;
+      }
+      if (m0 != -INFINITY) s0 += ex2((xv - m0) * c);
+    }
+  }
+  softmax_merge(m0, s0, m1, s1, c);
+  m = m0;
+  s = s0;
 }
 
 template <typename TT, int NT, int MINB>
@@ -637,33 +675,9 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     }
 
     // ---- sweep 1: (max, sum) ------------------------------------------------
-    float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
-    if (vec) {
-      const uint4* rv = reinterpret_cast<const uint4*>(row);
-      const int nv = V / kEl;
-      int j = tid;
-      for (; j + 7 * NT < nv; j += 8 * NT) {   // 8 vectors (128 B) in flight per thread
-        uint4 a[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) a[u] = ldg_hint(rv + j + u * NT, keep);
-#pragma unroll
-        for (int u = 0; u < 8; u += 2) {
-          softmax_acc16<TT>(a[u], m0, s0, P.c);
-          softmax_acc16<TT>(a[u + 1], m1, s1, P.c);
-        }
-      }
-      for (; j < nv; j += NT) softmax_acc16<TT>(ldg_hint(rv + j, keep), m0, s0, P.c);
-    } else {
-      for (int v = tid; v < V; v += NT) {
-        const float xv = load_logit(row + v);
-        if (xv > m0) {
-          s0 *= ex2((m0 - xv) * P.c);
-          m0 = xv;
-        }
-        if (m0 != -INFINITY) s0 += ex2((xv - m0) * P.c);
-      }
-    }
-    softmax_merge(m0, s0, m1, s1, P.c);
+    const int hi = vec ? V / kEl : V;
+    float m0, s0;
+    sweep1<TT, NT>(row, 0, hi, vec, P.c, keep, m0, s0);
     warp_softmax(m0, s0, P.c);
     if (lane == 0) red[par][warp] = make_float4(m0, s0, 0.f, 0.f);
     __syncthreads();
@@ -697,11 +711,11 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     float beta = 0.0f;
     Race best = race_none();
     if (has_q && race)
-      sweep2<TT, NT, true, true>(row, qrow, V, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, true, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
     else if (has_q)
-      sweep2<TT, NT, true, false>(row, qrow, V, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, true, false>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
     else if (race)
-      sweep2<TT, NT, false, true>(row, qrow, V, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, false, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
     beta = warp_sum(beta);
     warp_race(best);
     if (lane == 0) red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
@@ -733,6 +747,241 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     // s_slot / s_dec / red[par] are rewritten next iteration only after the
     // __syncthreads that follows thread 0's next slot grab.
   }
+}
+
+// ---------------------------------------------------------------------------
+// Pair row kernel (T > 0): the sweep kernel with every row split over a cluster
+// of two CTAs (512 threads each, two CTAs per SM).  Rank 0 takes the work slot
+// and sends it to both CTAs; each CTA sweeps half of the row; the halves'
+// (max, sum) and rank 0's view of the request's earlier rows are exchanged
+// through distributed shared memory, so both CTAs take the same accept / race
+// decision; the halves' beta and race candidates go to rank 0, which writes the
+// outputs.  Half as many rows are live in L2 between their two sweeps as with
+// one row per CTA at the same number of threads per SM.
+// ---------------------------------------------------------------------------
+struct alignas(16) PairShared {
+  uint64_t bdesc[2];   // work slot arrived (1 arrival, from rank 0)
+  uint64_t bms[2];     // both halves' (max, sum) arrived (2 arrivals)
+  uint64_t bred[2];    // both halves' (beta, race) arrived at rank 0 (2 arrivals)
+  float4 desc[2];      // (slot lo bits, slot hi bits, prefix at grab, -)
+  float4 ms[2][2];     // [parity][rank] (max, sum, rank 0's prefix, -)
+  float4 part[2][2];   // [parity][rank] (beta, race w, race e, race index)
+  float4 red[2][16];
+  float dec[4];        // max, sum, flags, -
+  float acc_x[2];      // p(x), q(x)
+  int gmax, bad, flag;
+};
+
+template <typename TT>
+__global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
+  constexpr int NT = 512, NW = 16;
+  constexpr int kEl = 16 / sizeof(TT);
+  __shared__ PairShared S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t cid = cluster_id_x();
+  const int B = P.B, V = P.V;
+  const bool vec = P.vec_ok != 0;
+
+  if (tid == 0) {
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(smem_addr(&S.bdesc[p]), 1);
+      mbar_init(smem_addr(&S.bms[p]), 2);
+      mbar_init(smem_addr(&S.bred[p]), 2);
+    }
+    S.gmax = 0;
+    S.bad = 0;
+    S.flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  {
+    int gm = 0, bad = 0;
+    for (int b = tid; b < B; b += NT) {
+      const int g = __ldg(P.cu + b + 1) - __ldg(P.cu + b);
+      gm = max(gm, g);
+      bad |= (g < 0);
+    }
+    if (gm) atomicMax(&S.gmax, gm);
+    if (bad) atomicOr(&S.bad, 1);
+  }
+  cluster_sync_all();
+  if (cid == 0 && rank == 0 && tid == 0) {
+    if (S.bad || __ldg(P.cu) != 0) set_err(P.err, SPECDEC_DEVERR_BAD_CU);
+    *P.defer_count = 0;
+  }
+  const int64_t total = (int64_t)B * (S.gmax + 1);
+  const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+  const int nunits = vec ? V / kEl : V;
+  const int half = (nunits + 1) / 2;
+  const int lo = rank ? half : 0, hi = rank ? nunits : half;
+  bool ok = true;
+
+  for (uint32_t k = 0;; ++k) {
+    const int par = k & 1;
+    const uint32_t ph = (k >> 1) & 1;
+    // ---- rank 0 takes the next slot and sends it to both CTAs ---------------
+    if (rank == 0 && tid == 0) {
+      long long u;
+      int prefix = kPrefixAllAccepted;
+      while (true) {
+        u = (long long)atomicAdd(P.sched, 1ull);
+        if (u >= total) {
+          u = -1;
+          break;
+        }
+        const int i = (int)(u / B), b = (int)(u % B);
+        const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+        if (i > g) continue;
+        const int64_t t = (int64_t)c0 + b + i;
+        if (t >= P.cap_rows) {
+          set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+          continue;
+        }
+        prefix = i > 0 ? read_prefix(P.status, t - i, i, P.epoch) : kPrefixAllAccepted;
+        if (i == g && prefix == kPrefixRejected) continue;  // bonus row nobody needs
+        break;
+      }
+      const uint32_t slot = smem_addr(&S.desc[par]);
+      for (uint32_t r = 0; r < 2; ++r) {
+        st_cluster_v4(mapa(slot, r), __int_as_float((int)(u & 0xFFFFFFFF)),
+                      __int_as_float((int)(u >> 32)), __int_as_float(prefix), 0.f);
+        mbar_arrive_cluster(mapa(smem_addr(&S.bdesc[par]), r));
+      }
+    }
+    if (tid == 0) S.flag = (ok && mbar_wait_cluster(smem_addr(&S.bdesc[par]), ph)) ? 0 : 1;
+    __syncthreads();
+    if (S.flag) {
+      ok = false;
+      break;
+    }
+    const float4 dsc = S.desc[par];
+    const long long u = (long long)(((unsigned long long)(uint32_t)__float_as_int(dsc.y) << 32) |
+                                    (uint32_t)__float_as_int(dsc.x));
+    if (u < 0) break;
+    const int prefix0 = __float_as_int(dsc.z);
+    const int i = (int)(u / B), b = (int)(u % B);
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t = (int64_t)c0 + b + i, d = (int64_t)c0 + i;
+    const bool has_q = i < g;
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    const float* qrow = has_q ? P.q + d * (int64_t)V : nullptr;
+
+    int x = -1;
+    float lx = 0.0f, qx = 0.0f;
+    bool valid = true;
+    if (tid == 0 && has_q) {
+      x = __ldg(P.ids + d);
+      valid = (x >= 0 && x < V);
+      if (valid) {
+        lx = load_logit(row + x);
+        qx = __ldg(qrow + x);
+      }
+    }
+
+    // ---- sweep 1 over this CTA's half -----------------------------------------
+    float m0, s0;
+    sweep1<TT, NT>(row, lo, hi, vec, P.c, keep, m0, s0);
+    warp_softmax(m0, s0, P.c);
+    if (lane == 0) S.red[0][warp] = make_float4(m0, s0, 0.f, 0.f);
+    __syncthreads();
+    if (tid == 0) {
+      float mh = -INFINITY, sh = 0.0f;
+      for (int w = 0; w < NW; ++w) softmax_merge(mh, sh, S.red[0][w].x, S.red[0][w].y, P.c);
+      int pfx = prefix0;
+      if (rank == 0 && pfx == kPrefixUnknown) pfx = read_prefix(P.status, t - i, i, P.epoch);
+      const uint32_t slot = smem_addr(&S.ms[par][rank]);
+      for (uint32_t r = 0; r < 2; ++r) {
+        st_cluster_v4(mapa(slot, r), mh, sh, __int_as_float(pfx), 0.f);
+        mbar_arrive_cluster(mapa(smem_addr(&S.bms[par]), r));
+      }
+      ok = mbar_wait_cluster(smem_addr(&S.bms[par]), ph);
+      float M = -INFINITY, Ssum = 0.0f;
+      softmax_merge(M, Ssum, S.ms[par][0].x, S.ms[par][0].y, P.c);
+      softmax_merge(M, Ssum, S.ms[par][1].x, S.ms[par][1].y, P.c);
+      const int prefix = __float_as_int(S.ms[par][0].z);
+      const float invS = 1.0f / Ssum;
+      float px = 0.0f;
+      bool acc = false;
+      if (has_q) {
+        if (valid) px = ex2((lx - M) * P.c) * invS;
+        const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
+        acc = accept_test(r, px, qx);
+      }
+      const bool race = (prefix == kPrefixAllAccepted) && (!has_q || !acc);
+      S.dec[0] = M;
+      S.dec[1] = Ssum;
+      S.dec[2] = __int_as_float((acc ? 1 : 0) | (race ? 2 : 0) | (valid ? 0 : 4) | (ok ? 0 : 8));
+      S.acc_x[0] = px;
+      S.acc_x[1] = qx;
+    }
+    __syncthreads();
+    const float M = S.dec[0], Ssum = S.dec[1];
+    const int flags = __float_as_int(S.dec[2]);
+    if (flags & 8) {
+      ok = false;
+      break;
+    }
+    const float invS = 1.0f / Ssum;
+    const bool acc = flags & 1, race = flags & 2;
+    const bool resid = has_q && !acc;
+    const uint64_t rkey = stream_key(P.seed, P.req_offset + b, i, 1);
+
+    // ---- sweep 2 over this CTA's half -----------------------------------------
+    float beta = 0.0f;
+    Race best = race_none();
+    if (has_q && race)
+      sweep2<TT, NT, true, true>(row, qrow, lo, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+    else if (has_q)
+      sweep2<TT, NT, true, false>(row, qrow, lo, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+    else if (race)
+      sweep2<TT, NT, false, true>(row, qrow, lo, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+    beta = warp_sum(beta);
+    warp_race(best);
+    if (lane == 0) S.red[1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
+    __syncthreads();
+    if (tid == 0) {
+      float bh = 0.0f;
+      Race rh = race_none();
+      for (int w = 0; w < NW; ++w) {
+        const float4 r4 = S.red[1][w];
+        bh += r4.x;
+        race_merge(rh, r4.y, r4.z, __float_as_int(r4.w));
+      }
+      st_cluster_v4(mapa(smem_addr(&S.part[par][rank]), 0), bh, rh.w, rh.e, __int_as_float(rh.idx));
+      mbar_arrive_cluster(mapa(smem_addr(&S.bred[par]), 0));
+      if (rank == 0) {
+        ok = mbar_wait_cluster(smem_addr(&S.bred[par]), ph);
+        float bt = 0.0f;
+        Race tb = race_none();
+        for (int r = 0; r < 2; ++r) {
+          const float4 r4 = S.part[par][r];
+          bt += r4.x;
+          race_merge(tb, r4.y, r4.z, __float_as_int(r4.w));
+        }
+        if (ok) {
+          P.row_stats[t] = make_float2(M, Ssum);
+          uint32_t stw = kStDone;
+          if (has_q) {
+            if (flags & 4) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+            if (acc) stw |= kStAccepted;
+            if (P.out_beta) P.out_beta[d] = bt;
+            if (P.out_px) P.out_px[d] = S.acc_x[0];
+            if (P.out_qx) P.out_qx[d] = S.acc_x[1];
+            if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+          }
+          if (race && tb.w > 0.0f) {
+            P.out_tokens[t] = tb.idx;
+            stw |= kStRaceDone;
+          }
+          st_relaxed_u64(P.status + t, make_status(P.epoch, stw));
+        }
+      }
+    }
+  }
+  if (!ok && tid == 0) set_err(P.err, SPECDEC_DEVERR_TIMEOUT);
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still write to its shared memory
 }
 
 // ---------------------------------------------------------------------------

@@ -55,6 +55,7 @@ struct specdec_ctx {
   int smem_per_sm = 0;
   int sweep_threads = 512;      // block size of the sweep kernel (1024 x 1, 512 x 2, 256 x 4 per SM)
   int stream_ctas = 1;          // stream kernel CTAs per SM (1 or 2)
+  int pair_clusters[2] = {0, 0};  // co-resident 2-CTA clusters of pair_row_kernel<f32 / bf16>
   int occ_cache[2][5][2] = {};  // [dtype][cluster index] -> {smem, clusters}
 };
 
@@ -186,7 +187,30 @@ template <typename TT>
 int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, cudaStream_t st) {
   const int B = P.B;
   if (h->ev_before) cudaEventRecord(h->ev_before, st);
-  if (path == SPECDEC_PATH_STREAM) {
+  if (path == SPECDEC_PATH_PAIR) {
+    int& nclus = h->pair_clusters[sizeof(TT) == 2];
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(512);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    if (nclus == 0) {
+      cfg.gridDim = dim3(2 * h->num_sms);
+      if (cudaOccupancyMaxActiveClusters(&nclus, pair_row_kernel<TT>, &cfg) != cudaSuccess || nclus <= 0) {
+        cudaGetLastError();
+        nclus = 0;
+        return SPECDEC_ERR_CUDA;
+      }
+    }
+    cfg.gridDim = dim3(2 * nclus);
+    if (cudaLaunchKernelEx(&cfg, pair_row_kernel<TT>, P) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  } else if (path == SPECDEC_PATH_STREAM) {
     const int ctas = h->stream_ctas;
     const int fixed = (int)((sizeof(StreamShared) + 127) / 128 * 128);
     const int budget = ctas == 1 ? h->smem_optin : h->smem_per_sm / 2 - 1024;
@@ -365,7 +389,7 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
     if (!f.ok) path = SPECDEC_PATH_SWEEP;
   }
   h->last_path = path;
-  h->last_cluster = path == SPECDEC_PATH_FUSED ? f.C : 0;
+  h->last_cluster = path == SPECDEC_PATH_FUSED ? f.C : (path == SPECDEC_PATH_PAIR ? 2 : 0);
   return dtype == SPECDEC_BF16 ? launch_sampling<__nv_bfloat16>(h, P, f, path, st)
                                : launch_sampling<float>(h, P, f, path, st);
 }
@@ -394,7 +418,7 @@ int specdec_get_error(specdec_handle_t h, int* device_error, void* stream) {
 }
 
 int specdec_set_path(specdec_handle_t h, int path) {
-  if (!h || path < SPECDEC_PATH_AUTO || path > SPECDEC_PATH_STREAM || path == SPECDEC_PATH_GREEDY)
+  if (!h || path < SPECDEC_PATH_AUTO || path > SPECDEC_PATH_PAIR || path == SPECDEC_PATH_GREEDY)
     return SPECDEC_ERR_INVALID_ARG;
   h->path_override = path;
   return SPECDEC_OK;
