@@ -44,7 +44,10 @@
  *     iff x_i == g_i, beta_i = [x_i == g_i], t = g_n;
  *   - beta is emitted for every draft position, also after the first reject;
  *   - a draft id outside [0, V) is treated as rejected with p(x) = q(x) = 0 and
- *     the call reports ORACLE_BAD_DRAFT_ID.
+ *     the call reports ORACLE_BAD_DRAFT_ID;
+ *   - no draft probabilities at T > 0 means a one-hot drafter (the "greedy"
+ *     draft sampling of the vllbc page's Section 2.2 note): q_i is the indicator
+ *     of x_i, written out as such and run through the same steps.
  *
  * Counter-based generator (the pages only say "uniform random"): SplitMix64
  * (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
@@ -165,8 +168,8 @@ static int argmax_row(const void* logits, int dtype, size_t row, int V) {
 /*
  * Verifies one request b with gamma drafts.
  *   tgt    : the request's gamma+1 target logit rows, row-major [gamma+1, V]
- *   draft  : the request's gamma draft probability rows [gamma, V] (ignored, and
- *            may be NULL, when T == 0)
+ *   draft  : the request's gamma draft probability rows [gamma, V]; ignored when
+ *            T == 0; NULL at T > 0 means a one-hot drafter (q_i = [v == x_i])
  *   ids    : the gamma draft token ids
  * Outputs (any may be NULL):
  *   tokens [gamma+1]  accepted drafts, then the correction / bonus token, then -1
@@ -226,6 +229,20 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
       free(acc);
       free(tie);
       return ORACLE_OOM;
+    }
+    /* A one-hot drafter: q_i(v) = [v == x_i], materialised row by row. */
+    float* onehot = NULL;
+    if (!draft && gamma > 0) {
+      onehot = (float*)calloc((size_t)gamma * (size_t)V, sizeof(float));
+      if (!onehot) {
+        free(p);
+        free(acc);
+        free(tie);
+        return ORACLE_OOM;
+      }
+      for (int i = 0; i < gamma; ++i)
+        if (ids[i] >= 0 && ids[i] < V) onehot[(size_t)i * (size_t)V + (size_t)ids[i]] = 1.0f;
+      draft = onehot;
     }
     /* Accept test and beta at every draft position. */
     for (int i = 0; i < gamma; ++i) {
@@ -304,6 +321,7 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
     if (k2 > -INFINITY && (k1 - k2) <= NEAR_TIE_REL * k1) req_tie = 1;
     free(w);
     free(p);
+    free(onehot);
   }
 
   if (tokens) {
@@ -341,7 +359,6 @@ int oracle_rejection_sample(const void* target_logits, int dtype, const float* d
   if (B <= 0 || V <= 0 || !target_logits || !draft_ids || !cu) return ORACLE_INVALID_ARG;
   if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
   if (!(T >= 0.0) || isinf(T)) return ORACLE_INVALID_ARG;
-  if (T > 0.0 && !draft_probs) return ORACLE_INVALID_ARG;
   if (cu[0] != 0) return ORACLE_INVALID_ARG;
   for (int b = 0; b < B; ++b)
     if (cu[b + 1] < cu[b]) return ORACLE_INVALID_ARG;
@@ -352,7 +369,7 @@ int oracle_rejection_sample(const void* target_logits, int dtype, const float* d
     int d0 = cu[b], gamma = cu[b + 1] - cu[b];
     size_t t0 = (size_t)d0 + (size_t)b;
     const void* tgt = (const char*)target_logits + t0 * (size_t)V * esize;
-    const float* dr = (T > 0.0) ? draft_probs + (size_t)d0 * (size_t)V : NULL;
+    const float* dr = (T > 0.0 && draft_probs) ? draft_probs + (size_t)d0 * (size_t)V : NULL;
     int s = oracle_verify_request(
         b, gamma, tgt, dtype, dr, draft_ids + d0, V, T, seed, out_tokens ? out_tokens + t0 : NULL,
         out_num_accepted ? out_num_accepted + b : NULL, out_beta ? out_beta + d0 : NULL,

@@ -126,7 +126,6 @@ def test_invalid_arguments():
     q = np.full((1, 4), 0.25, np.float32)
     assert _run(tgt, q, [0], T=-1.0).status == oracle.INVALID_ARG
     assert _run(tgt, q, [0], T=float("nan")).status == oracle.INVALID_ARG
-    assert _run(tgt, None, [0], T=1.0).status == oracle.INVALID_ARG
     r = oracle.rejection_sample(np.zeros((4, 4), np.float32), np.full((2, 4), .25, np.float32),
                                 np.zeros(2, np.int32), np.array([0, 1, 2], np.int32), 1.0, 0)
     assert r.status == oracle.OK
@@ -187,3 +186,30 @@ def test_greedy_brute_force_with_ties(dtype):
         assert all(t == -1 for t in toks[n + 1:])
         assert list(r.beta[b * gamma:(b + 1) * gamma]) == [float(a) for a in acc]
     assert r.near_tie.sum() == 0
+
+
+# ----------------------------------------------------------------------------
+# One-hot drafter (no draft probabilities at T > 0): q_i = [v == x_i].
+# ----------------------------------------------------------------------------
+
+def test_onehot_draft_closed_forms():
+    # beta = sum min(p, onehot(x)) = p(x); q(x) = 1; the accept test is r < p(x).
+    rng = np.random.default_rng(8)
+    V, gamma, T = 9, 4, 0.7
+    logits = rng.normal(0, 2, size=(gamma + 1, V)).astype(np.float32)
+    ids = rng.integers(0, V, size=gamma)
+    for seed in range(20):
+        r = _run(logits, None, ids, T=T, seed=seed)
+        assert r.status == 0
+        for i in range(gamma):
+            l = logits[i].astype(np.float64) / T
+            p = np.exp(l - l.max())
+            p /= p.sum()
+            assert r.beta[i] == pytest.approx(p[ids[i]], abs=1e-12)
+            assert r.q_x[i] == 1.0 and r.p_x[i] == pytest.approx(p[ids[i]], abs=1e-12)
+            u = oracle.uniform(seed, 0, i, 0, 0, 1)[0]
+            if abs(u - p[ids[i]]) > 1e-9:
+                assert r.accept[i] == int(u < p[ids[i]])
+        n = r.num_accepted[0]
+        if n < gamma:
+            assert r.tokens[n] != ids[n]          # the residual excludes the draft token

@@ -103,3 +103,24 @@ def test_pins_detect_a_planted_mistake():
     except AssertionError:
         detected = True
     assert detected
+
+
+def test_a_onehot_drafter_output_distribution():
+    # A deterministic (greedy) drafter is q = onehot(x): the emitted token still
+    # follows p, and the acceptance rate is p(x).
+    from scipy import stats  # noqa: F401
+    rng = np.random.default_rng(21)
+    n, V = 400_000, 8
+    lt = np.array([[0.3, -1.0, 1.2, 0.0, 0.7, -0.4, 0.5, -2.0],
+                   [1.0, 0.2, -0.5, 0.9, 0.0, -1.5, 0.4, 0.1]], np.float32)
+    x = 2
+    tgt = np.tile(lt, (n, 1))
+    ids = np.full(n, x, np.int32)
+    cu = np.arange(n + 1).astype(np.int32)
+    r = oracle.rejection_sample(tgt, None, ids, cu, 1.0, 5)
+    assert r.status == 0
+    p = sc.softmax64(lt, 1.0)
+    tok0 = r.tokens.reshape(n, 2)[:, 0]
+    assert sc.chi2_ok(np.bincount(tok0, minlength=V), p[0]) > sc.P_MIN
+    acc = r.accept.mean()
+    assert abs(acc - p[0, x]) < 3 * np.sqrt(p[0, x] * (1 - p[0, x]) / n)
