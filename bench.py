@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--vocab", type=int, default=None, help="override V")
     ap.add_argument("--path", choices=["auto", "fused", "sweep", "stream", "pair", "two_pass"],
                     default="auto")
+    ap.add_argument("--draft", choices=["probs", "onehot"], default="probs",
+                    help="onehot: no draft rows (a greedy drafter, q = one-hot at the draft id)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -242,6 +244,9 @@ def main():
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     w = make_config(args.config, device=dev, B=args.batch, V=args.vocab)
+    if args.draft == "onehot":
+        w.draft_probs = None
+        w.name += " one-hot drafts"
     esize = 2 if w.dtype == "bf16" else 4
     tgt_bytes = w.n_target * w.V * esize
     drf_bytes = 0 if w.draft_probs is None else w.n_draft * w.V * 4

@@ -111,8 +111,12 @@ int specdec_reserve(specdec_handle_t h, int64_t max_draft_positions, int max_bat
  *                      single-pass path, other strides a two-pass path
  *   dtype              SPECDEC_F32 or SPECDEC_BF16
  *   draft_probs        device [N_d, V] float32 rows of q (taken as given, not
- *                      renormalised); ignored and may be NULL when T == 0, a
- *                      valid pointer otherwise (even when N_d == 0)
+ *                      renormalised); ignored when T == 0.  NULL at T > 0 means
+ *                      a one-hot ("greedy") drafter, q_i = [v == x_i] (the
+ *                      vllbc page's Section 2.2 note on vLLM's draft sampling):
+ *                      beta_i = p_i(x_i), accept iff r_i < p_i(x_i), and the
+ *                      correction is drawn from p with x removed; no draft row
+ *                      is read
  *   draft_ids          device [N_d] int32 (a valid pointer even when N_d == 0)
  *   cu_num_draft_tokens device [B+1] int32, cu[0] = 0, non-decreasing
  *   B, V               requests (>= 1) and vocabulary size (1 .. 2^30)

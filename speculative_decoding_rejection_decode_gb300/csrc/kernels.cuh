@@ -468,7 +468,7 @@ __device__ __forceinline__ void softmax_acc16(const uint4& w, float& m, float& s
 template <bool kHasQ, bool kRace>
 __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float M, float c,
                                          float invS, bool resid, uint64_t rkey, uint32_t v,
-                                         float& beta, Race& best) {
+                                         float& beta, Race& best, int excl = -1) {
   const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
   float p[4];
 #pragma unroll
@@ -483,8 +483,11 @@ __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float
 #pragma unroll
     for (int k = 0; k < 4; ++k) e[k] = neg_log_uniform(kb[k]);
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      race_merge(best, (kHasQ && resid) ? fmaxf(p[k] - qv[k], 0.0f) : p[k], e[k], (int32_t)(v + k));
+    for (int k = 0; k < 4; ++k) {
+      float w = (kHasQ && resid) ? fmaxf(p[k] - qv[k], 0.0f) : p[k];
+      if (!kHasQ && (int)(v + k) == excl) w = 0.0f;  // one-hot draft: residual is p without x
+      race_merge(best, w, e[k], (int32_t)(v + k));
+    }
   }
 }
 
@@ -493,7 +496,7 @@ __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float
 template <typename TT, int NT, bool kHasQ, bool kRace>
 __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo, int hi, bool vec,
                                        float M, float c, float invS, bool resid, uint64_t rkey,
-                                       uint64_t pol, float& beta, Race& best) {
+                                       uint64_t pol, float& beta, Race& best, int excl = -1) {
   constexpr int kEl = 16 / sizeof(TT);
   // target vectors loaded per iteration: fewer where the race needs registers
   constexpr int U = kRace ? 2 : (sizeof(TT) == 2 ? 3 : 4);
@@ -524,7 +527,7 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
           float4 q4 = zero4;
           if constexpr (kHasQ) q4 = *reinterpret_cast<const float4*>(&b[u][h]);
           sweep2_4<kHasQ, kRace>(x + 4 * h, q4, M, c, invS, resid, rkey,
-                                 (uint32_t)((j + u * NT) * kEl + 4 * h), beta, best);
+                                 (uint32_t)((j + u * NT) * kEl + 4 * h), beta, best, excl);
         }
       }
     }
@@ -539,7 +542,7 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
           q4 = *reinterpret_cast<const float4*>(&w);
         }
         sweep2_4<kHasQ, kRace>(x + 4 * h, q4, M, c, invS, resid, rkey, (uint32_t)(j * kEl + 4 * h),
-                               beta, best);
+                               beta, best, excl);
       }
     }
   } else {
@@ -550,7 +553,9 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
         qv = __ldg(qrow + v);
         beta += fminf(p, qv);
       }
-      if constexpr (kRace) race_offer(best, (kHasQ && resid) ? fmaxf(p - qv, 0.0f) : p, rkey, (uint32_t)v);
+      if constexpr (kRace)
+        race_offer(best, (kHasQ && resid) ? fmaxf(p - qv, 0.0f) : (v == excl ? 0.0f : p), rkey,
+                   (uint32_t)v);
     }
   }
 }
@@ -597,7 +602,7 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
   constexpr int kEl = 16 / sizeof(TT);
   __shared__ float4 red[2][NW];
   __shared__ long long s_slot;
-  __shared__ int s_gmax, s_bad, s_prefix;
+  __shared__ int s_gmax, s_bad, s_prefix, s_x;
   __shared__ float s_dec[4];  // px, qx, flags
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B, V = P.V;
@@ -657,8 +662,10 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
     const int64_t t = (int64_t)c0 + b + i, d = (int64_t)c0 + i;
     const bool has_q = i < g;
+    // no draft rows: a one-hot drafter, q_i = [v == x_i] (never read)
+    const bool onehot = P.q == nullptr;
     const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
-    const float* qrow = has_q ? P.q + d * (int64_t)V : nullptr;
+    const float* qrow = (has_q && !onehot) ? P.q + d * (int64_t)V : nullptr;
     const int par = it & 1;
 
     // thread 0 fetches what the accept test needs while sweep 1 runs
@@ -670,8 +677,9 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
       valid = (x >= 0 && x < V);
       if (valid) {
         lx = load_logit(row + x);
-        qx = __ldg(qrow + x);
+        qx = onehot ? 1.0f : __ldg(qrow + x);
       }
+      s_x = x;
     }
 
     // ---- sweep 1: (max, sum) ------------------------------------------------
@@ -708,14 +716,17 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     const uint64_t rkey = stream_key(P.seed, P.req_offset + b, i, 1);
 
     // ---- sweep 2: beta and the race ---------------------------------------
+    // (a one-hot draft needs no sweep for beta = p(x); only the race reads the
+    // row again, with x removed from a correction's residual)
     float beta = 0.0f;
     Race best = race_none();
-    if (has_q && race)
+    if (has_q && !onehot && race)
       sweep2<TT, NT, true, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
-    else if (has_q)
+    else if (has_q && !onehot)
       sweep2<TT, NT, true, false>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
     else if (race)
-      sweep2<TT, NT, false, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, false, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best,
+                                  resid ? s_x : -1);
     beta = warp_sum(beta);
     warp_race(best);
     if (lane == 0) red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
@@ -733,7 +744,7 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
       if (has_q) {
         if (flags & 4) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
         if (acc) st |= kStAccepted;
-        if (P.out_beta) P.out_beta[d] = bt;
+        if (P.out_beta) P.out_beta[d] = onehot ? s_dec[0] : bt;
         if (P.out_px) P.out_px[d] = s_dec[0];
         if (P.out_qx) P.out_qx[d] = s_dec[1];
         if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
@@ -1465,13 +1476,16 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
     const float2 ms = P.row_stats[t];
     const float invS = 1.0f / ms.y;
     const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
-    const float* qrow = has_q ? P.q + ((int64_t)c0 + n) * (int64_t)V : nullptr;
+    const bool onehot = P.q == nullptr;
+    const float* qrow = (has_q && !onehot) ? P.q + ((int64_t)c0 + n) * (int64_t)V : nullptr;
+    const int excl = (has_q && onehot) ? __ldg(P.ids + c0 + n) : -1;  // residual of a one-hot draft
     const uint64_t rkey = stream_key(P.seed, P.req_offset + b, n, 1);
     const int v0 = sl * P.rslice_len, v1 = min(V, v0 + P.rslice_len);
     Race best = race_none();
     for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
       const float p = ex2((load_logit(row + v) - ms.x) * P.c) * invS;
-      race_offer(best, has_q ? fmaxf(p - __ldg(qrow + v), 0.0f) : p, rkey, (uint32_t)v);
+      const float w = qrow ? fmaxf(p - __ldg(qrow + v), 0.0f) : (v == excl ? 0.0f : p);
+      race_offer(best, w, rkey, (uint32_t)v);
     }
     const Race tb = block_race<TT>(best, red);
     if (threadIdx.x == 0) {

@@ -86,7 +86,6 @@ extern "C" int specdec_rejection_sample_noalloc(
   if (!std::isfinite(T) || T < 0.0f) return SPECDEC_ERR_INVALID_ARG;
   if (!target_logits || !draft_ids || !cu_num_draft_tokens || !out_tokens || !out_num_accepted)
     return SPECDEC_ERR_INVALID_ARG;
-  if (T > 0.0f && !draft_probs) return SPECDEC_ERR_INVALID_ARG;
   if (B > kBatch || n_draft_positions + B > kRows) return SPECDEC_ERR_CAPACITY;
 
   unsigned char* base = nullptr;

@@ -329,7 +329,6 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
   if (!std::isfinite(T) || T < 0.0f) return SPECDEC_ERR_INVALID_ARG;
   if (!target_logits || !draft_ids || !cu_num_draft_tokens || !out_tokens || !out_num_accepted)
     return SPECDEC_ERR_INVALID_ARG;
-  if (T > 0.0f && !draft_probs) return SPECDEC_ERR_INVALID_ARG;
   if (cudaSetDevice(h->device) != cudaSuccess) return SPECDEC_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = ensure_capacity(h, cu_num_draft_tokens, B, st);
@@ -381,6 +380,7 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
              reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
   P.sched = reinterpret_cast<unsigned long long*>(h->small + 2);
   int path = h->path_override == SPECDEC_PATH_AUTO ? SPECDEC_PATH_SWEEP : h->path_override;
+  if (!draft_probs) path = SPECDEC_PATH_SWEEP;  // one-hot drafts: the sweep kernel handles them
   if (path == SPECDEC_PATH_STREAM && !P.vec_ok) path = SPECDEC_PATH_SWEEP;
   FusedConfig f;
   if (path == SPECDEC_PATH_FUSED) {

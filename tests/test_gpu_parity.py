@@ -317,7 +317,7 @@ def test_host_argument_errors(V):
     for k, v, want in (("B", 0, SPECDEC_ERR_INVALID_ARG), ("V", 0, SPECDEC_ERR_INVALID_ARG),
                        ("T", -1.0, SPECDEC_ERR_INVALID_ARG), ("T", float("nan"), SPECDEC_ERR_INVALID_ARG),
                        ("T", float("inf"), SPECDEC_ERR_INVALID_ARG), ("dtype", 7, SPECDEC_ERR_UNSUPPORTED_DTYPE),
-                       ("draft_probs", None, SPECDEC_ERR_INVALID_ARG), ("h", None, SPECDEC_ERR_INVALID_ARG),
+                       ("h", None, SPECDEC_ERR_INVALID_ARG),
                        ("out_tokens", None, SPECDEC_ERR_INVALID_ARG)):
         args = dict(base)
         args[k] = v
@@ -356,3 +356,39 @@ def test_stat_a_joint_two_tokens(V):
 def test_stat_c_eq1(V):
     out = sc.check_c_eq1(numpy_runner(V))
     assert out["pvalue"] > sc.P_MIN and out["z"] < 3.0
+
+
+# --------------------------------------------------------------------------
+# one-hot ("greedy") drafts at T > 0: no draft rows
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Vsz,dtype,T", [(32000, "f32", 1.0), (128256, "bf16", 0.8), (5003, "f32", 1.3),
+                                         (256000, "bf16", 1.0)])
+def test_onehot_drafts_parity(V, Vsz, dtype, T):
+    w = make_workload(name="onehot", B=48, gamma=(0, 7), V=Vsz, dtype=dtype, T=T, seed=61,
+                      ids="argmax0.75", device="cuda")
+    assert w.draft_probs is None
+    g = run_gpu(V, w)
+    assert V.get_error() == 0
+    r = run_oracle(w)
+    st = compare(w, g, r)
+    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert np.all(g["q_x"] == 1.0)
+    assert np.abs(g["beta"] - g["p_x"]).max() <= 1e-6      # beta = p(x)
+
+
+def test_onehot_drafts_output_distribution(V):
+    # the emitted token follows p and the acceptance rate is p(x)
+    n, Vs, x = 300_000, 8, 2
+    lt = np.array([[0.3, -1.0, 1.2, 0.0, 0.7, -0.4, 0.5, -2.0],
+                   [1.0, 0.2, -0.5, 0.9, 0.0, -1.5, 0.4, 0.1]], np.float32)
+    tgt = torch.from_numpy(np.tile(lt, (n, 1))).cuda()
+    ids = torch.full((n,), x, dtype=torch.int32, device="cuda")
+    cu = torch.arange(n + 1, dtype=torch.int32, device="cuda")
+    out = V(tgt, None, ids, cu, 1.0, 9, extended=True, n_draft=n)
+    torch.cuda.synchronize()
+    p = sc.softmax64(lt, 1.0)
+    tok0 = out.tokens.cpu().numpy().reshape(n, 2)[:, 0]
+    assert sc.chi2_ok(np.bincount(tok0, minlength=Vs), p[0]) > sc.P_MIN
+    acc = out.accept.cpu().numpy().mean()
+    assert abs(acc - p[0, x]) < 3 * np.sqrt(p[0, x] * (1 - p[0, x]) / n)
