@@ -47,7 +47,18 @@
  *     the call reports ORACLE_BAD_DRAFT_ID;
  *   - no draft probabilities at T > 0 means a one-hot drafter (the "greedy"
  *     draft sampling of the vllbc page's Section 2.2 note): q_i is the indicator
- *     of x_i, written out as such and run through the same steps.
+ *     of x_i, written out as such and run through the same steps;
+ *   - top-k / top-p ([P4] Section 2.2: they fold into the adjusted p, like
+ *     temperature) restrict the target distribution of every row of a request
+ *     before the test: with e(v) = exp((L(v) - max L) / T),
+ *       top-k (1 <= k < V) keeps K = {v : fewer than k tokens have a larger
+ *         logit} (every token tied with the k-th largest logit stays);
+ *       top-p (P < 1) keeps v in K when A(v) = 0 or A(v) < P * S_K, where A(v)
+ *         sums e over the tokens with a larger logit and S_K sums e over K (the
+ *         smallest top set whose mass reaches P, ties at its edge included);
+ *       p'(v) = e(v) / (sum of e over the kept tokens) on the kept tokens, 0
+ *         elsewhere.  Draft probabilities are taken as already adjusted.
+ *     T == 0 ignores both (the argmax is always kept).
  *
  * Counter-based generator (the pages only say "uniform random"): SplitMix64
  * (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
@@ -63,7 +74,10 @@
  * differently from this double-precision one) are flagged per request:
  *   - an accept test with |r - min(1, ratio)| <= 1e-5 * max(r, min(1, ratio))
  *     at a tested position (0..n, or all positions when n == gamma);
- *   - a race whose two best keys k1 >= k2 satisfy k1 - k2 <= 1e-5 * k1.
+ *   - a race whose two best keys k1 >= k2 satisfy k1 - k2 <= 1e-5 * k1;
+ *   - a top-p edge with |A - P * S_K| <= 1e-5 * S_K for the last kept or the
+ *     first dropped group of equal logits, in a row 0..n (flagged per position
+ *     as well, since the whole adjusted row, beta included, depends on it).
  *
  * Parity pins (tests, CPU only): the splitmix64 published output for seed 0,
  * uniformity of U, softmax closed forms, beta by hand on tiny rows and its
@@ -147,6 +161,88 @@ static void softmax_row(const void* logits, int dtype, size_t row, int V, double
   for (int v = 0; v < V; ++v) p[v] /= sum;
 }
 
+/* A logit and its vocabulary index, for ordering a row. */
+typedef struct {
+  double l;
+  int v;
+} ranked_t;
+
+static int by_logit_desc(const void* a, const void* b) {
+  const ranked_t* x = (const ranked_t*)a;
+  const ranked_t* y = (const ranked_t*)b;
+  if (x->l > y->l) return -1;
+  if (x->l < y->l) return 1;
+  return (x->v > y->v) - (x->v < y->v);
+}
+
+/*
+ * The target distribution of one row after temperature, top-k and top-p (the
+ * adjusted p of [P4] Section 2.2; the kept sets are defined in the header
+ * comment).  top_k outside [1, V) and top_p >= 1 leave the softmax unchanged.
+ * Returns 1 when a top-p decision lies within the near-tie margin, else 0, or
+ * ORACLE_OOM.
+ */
+static int adjusted_row(const void* logits, int dtype, size_t row, int V, double T, int top_k,
+                        double top_p, double* p) {
+  const int use_k = top_k >= 1 && top_k < V;
+  const int use_p = !(top_p >= 1.0);
+  softmax_row(logits, dtype, row, V, T, p);
+  if (!use_k && !use_p) return 0;
+  ranked_t* r = (ranked_t*)malloc(sizeof(ranked_t) * (size_t)V);
+  if (!r) return ORACLE_OOM;
+  double mx = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    r[v].l = logit_at(logits, dtype, row * (size_t)V + (size_t)v);
+    r[v].v = v;
+    if (r[v].l > mx) mx = r[v].l;
+  }
+  qsort(r, (size_t)V, sizeof(ranked_t), by_logit_desc);
+  /* top-k: the kept prefix of the order ends with the group of the k-th logit */
+  int kend = V;
+  if (use_k) {
+    kend = top_k;
+    while (kend < V && r[kend].l == r[top_k - 1].l) ++kend;
+  }
+  /* S_K: the unnormalised mass e(v) = exp((L(v) - max L) / T) of K */
+  double s_k = 0.0;
+  for (int j = 0; j < kend; ++j) s_k += exp((r[j].l - mx) / T);
+  /* top-p: walk the groups of equal logits inside K */
+  int end = kend;
+  int tie = 0;
+  if (use_p) {
+    const double bound = top_p * s_k;
+    double above = 0.0;
+    int j = 0;
+    end = 0;
+    while (j < kend) {
+      int g = j;
+      double gm = 0.0;
+      while (g < kend && r[g].l == r[j].l) gm += exp((r[g++].l - mx) / T);
+      const int keep = (above == 0.0) || (above < bound);
+      if ((above > 0.0) && fabs(above - bound) <= NEAR_TIE_REL * s_k) tie = 1;
+      if (!keep) break;
+      end = g;
+      above += gm;
+      j = g;
+    }
+  }
+  /* zero the dropped tokens, renormalise over the kept ones */
+  double kept = 0.0;
+  for (int j = 0; j < end; ++j) kept += exp((r[j].l - mx) / T);
+  for (int j = end; j < V; ++j) p[r[j].v] = 0.0;
+  for (int j = 0; j < end; ++j) p[r[j].v] = exp((r[j].l - mx) / T) / kept;
+  free(r);
+  return tie;
+}
+
+/* Exported for the tests: the adjusted distribution of one row of V logits. */
+int oracle_adjusted_probs(const void* row, int dtype, int V, double T, int top_k, double top_p,
+                          double* p) {
+  if (!row || !p || V <= 0 || !(T > 0.0)) return ORACLE_INVALID_ARG;
+  if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
+  return adjusted_row(row, dtype, 0, V, T, top_k, top_p, p);
+}
+
 /* Greedy target token: first index of the largest stored value. */
 static int argmax_row(const void* logits, int dtype, size_t row, int V) {
   int best = 0;
@@ -179,13 +275,18 @@ static int argmax_row(const void* logits, int dtype, size_t row, int V) {
  *   accept [gamma]    the accept test at every position (also after the first
  *                     rejection, where it no longer affects the output)
  *   pos_near_tie [gamma]  accept-test near tie at that position
- *   near_tie [1]      request-level flag (tested positions or the race)
+ *   pos_adj_tie [gamma]   top-p near tie in that position's target row
+ *   near_tie [1]      request-level flag (tested positions, their top-p edges,
+ *                     the extra token's row or the race)
+ * top_k / top_p adjust every target row of the request (top_k outside [1, V)
+ * and top_p >= 1 switch them off; T == 0 ignores them).
  * Returns ORACLE_OK, ORACLE_BAD_DRAFT_ID or ORACLE_OOM.
  */
-int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, const float* draft,
-                          const int32_t* ids, int V, double T, uint64_t seed, int32_t* tokens,
-                          int32_t* num_accepted, double* beta, double* p_x, double* q_x,
-                          int32_t* accept, int32_t* pos_near_tie, int32_t* near_tie) {
+int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
+                              const float* draft, const int32_t* ids, int V, double T, int top_k,
+                              double top_p, uint64_t seed, int32_t* tokens, int32_t* num_accepted,
+                              double* beta, double* p_x, double* q_x, int32_t* accept,
+                              int32_t* pos_near_tie, int32_t* pos_adj_tie, int32_t* near_tie) {
   int status = ORACLE_OK;
   int n = gamma;
   int req_tie = 0;
@@ -223,6 +324,8 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
       }
     t = g[n];
     free(g);
+    if (pos_adj_tie)
+      for (int i = 0; i < gamma; ++i) pos_adj_tie[i] = 0;
   } else {
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     if (!p) {
@@ -245,9 +348,25 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
       draft = onehot;
     }
     /* Accept test and beta at every draft position. */
+    int* atie = (int*)calloc((size_t)(gamma + 1), sizeof(int));
+    if (!atie) {
+      free(onehot);
+      free(p);
+      free(acc);
+      free(tie);
+      return ORACLE_OOM;
+    }
     for (int i = 0; i < gamma; ++i) {
       const float* q = draft + (size_t)i * (size_t)V;
-      softmax_row(tgt, dtype, (size_t)i, V, T, p);
+      atie[i] = adjusted_row(tgt, dtype, (size_t)i, V, T, top_k, top_p, p);
+      if (atie[i] == ORACLE_OOM) {
+        free(atie);
+        free(onehot);
+        free(p);
+        free(acc);
+        free(tie);
+        return ORACLE_OOM;
+      }
       int x = ids[i];
       double px = 0.0, qx = 0.0;
       if (x >= 0 && x < V) {
@@ -279,17 +398,29 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
         n = i;
         break;
       }
-    for (int i = 0; i < gamma && i <= n; ++i) req_tie |= tie[i];
+    for (int i = 0; i < gamma && i <= n; ++i) req_tie |= tie[i] | atie[i];
 
     /* Correction (n < gamma) or bonus (n == gamma) distribution w. */
     double* w = (double*)malloc(sizeof(double) * (size_t)V);
     if (!w) {
+      free(atie);
+      free(onehot);
       free(p);
       free(acc);
       free(tie);
       return ORACLE_OOM;
     }
-    softmax_row(tgt, dtype, (size_t)n, V, T, p);
+    atie[gamma] = adjusted_row(tgt, dtype, (size_t)n, V, T, top_k, top_p, p);
+    if (atie[gamma] == ORACLE_OOM) {
+      free(w);
+      free(atie);
+      free(onehot);
+      free(p);
+      free(acc);
+      free(tie);
+      return ORACLE_OOM;
+    }
+    req_tie |= atie[gamma];
     if (n < gamma) {
       const float* q = draft + (size_t)n * (size_t)V;
       int any = 0;
@@ -319,6 +450,9 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
       }
     }
     if (k2 > -INFINITY && (k1 - k2) <= NEAR_TIE_REL * k1) req_tie = 1;
+    if (pos_adj_tie)
+      for (int i = 0; i < gamma; ++i) pos_adj_tie[i] = atie[i];
+    free(atie);
     free(w);
     free(p);
     free(onehot);
@@ -340,6 +474,16 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
   return status;
 }
 
+/* The request without top-k / top-p. */
+int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, const float* draft,
+                          const int32_t* ids, int V, double T, uint64_t seed, int32_t* tokens,
+                          int32_t* num_accepted, double* beta, double* p_x, double* q_x,
+                          int32_t* accept, int32_t* pos_near_tie, int32_t* near_tie) {
+  return oracle_verify_request_adj(b, gamma, tgt, dtype, draft, ids, V, T, 0, 1.0, seed, tokens,
+                                   num_accepted, beta, p_x, q_x, accept, pos_near_tie, NULL,
+                                   near_tie);
+}
+
 /* ---------------------------------------------------------------------- */
 /* Batch over a flattened ragged layout                                   */
 /* ---------------------------------------------------------------------- */
@@ -351,11 +495,13 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
  * row).  Output token slots follow the target rows.  Per-position outputs
  * follow the draft rows; near_tie is per request.  Any output may be NULL.
  */
-int oracle_rejection_sample(const void* target_logits, int dtype, const float* draft_probs,
-                            const int32_t* draft_ids, const int32_t* cu, int B, int V, double T,
-                            uint64_t seed, int32_t* out_tokens, int32_t* out_num_accepted,
-                            double* out_beta, double* out_p_x, double* out_q_x, int32_t* out_accept,
-                            int32_t* out_pos_near_tie, int32_t* out_near_tie) {
+int oracle_rejection_sample_adj(const void* target_logits, int dtype, const float* draft_probs,
+                                const int32_t* draft_ids, const int32_t* cu, int B, int V, double T,
+                                const int32_t* top_k, const double* top_p, uint64_t seed,
+                                int32_t* out_tokens, int32_t* out_num_accepted, double* out_beta,
+                                double* out_p_x, double* out_q_x, int32_t* out_accept,
+                                int32_t* out_pos_near_tie, int32_t* out_pos_adj_tie,
+                                int32_t* out_near_tie) {
   if (B <= 0 || V <= 0 || !target_logits || !draft_ids || !cu) return ORACLE_INVALID_ARG;
   if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
   if (!(T >= 0.0) || isinf(T)) return ORACLE_INVALID_ARG;
@@ -370,14 +516,26 @@ int oracle_rejection_sample(const void* target_logits, int dtype, const float* d
     size_t t0 = (size_t)d0 + (size_t)b;
     const void* tgt = (const char*)target_logits + t0 * (size_t)V * esize;
     const float* dr = (T > 0.0 && draft_probs) ? draft_probs + (size_t)d0 * (size_t)V : NULL;
-    int s = oracle_verify_request(
-        b, gamma, tgt, dtype, dr, draft_ids + d0, V, T, seed, out_tokens ? out_tokens + t0 : NULL,
+    int s = oracle_verify_request_adj(
+        b, gamma, tgt, dtype, dr, draft_ids + d0, V, T, top_k ? top_k[b] : 0,
+        top_p ? top_p[b] : 1.0, seed, out_tokens ? out_tokens + t0 : NULL,
         out_num_accepted ? out_num_accepted + b : NULL, out_beta ? out_beta + d0 : NULL,
         out_p_x ? out_p_x + d0 : NULL, out_q_x ? out_q_x + d0 : NULL,
         out_accept ? out_accept + d0 : NULL, out_pos_near_tie ? out_pos_near_tie + d0 : NULL,
-        out_near_tie ? out_near_tie + b : NULL);
+        out_pos_adj_tie ? out_pos_adj_tie + d0 : NULL, out_near_tie ? out_near_tie + b : NULL);
     if (s == ORACLE_OOM) return s;
     if (s != ORACLE_OK) status = s;
   }
   return status;
+}
+
+/* The batch without top-k / top-p. */
+int oracle_rejection_sample(const void* target_logits, int dtype, const float* draft_probs,
+                            const int32_t* draft_ids, const int32_t* cu, int B, int V, double T,
+                            uint64_t seed, int32_t* out_tokens, int32_t* out_num_accepted,
+                            double* out_beta, double* out_p_x, double* out_q_x, int32_t* out_accept,
+                            int32_t* out_pos_near_tie, int32_t* out_near_tie) {
+  return oracle_rejection_sample_adj(target_logits, dtype, draft_probs, draft_ids, cu, B, V, T, NULL,
+                                     NULL, seed, out_tokens, out_num_accepted, out_beta, out_p_x,
+                                     out_q_x, out_accept, out_pos_near_tie, NULL, out_near_tie);
 }

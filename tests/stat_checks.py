@@ -30,6 +30,27 @@ def softmax64(logits, T):
     return e / e.sum(axis=-1, keepdims=True)
 
 
+def adjusted64(logits, T, top_k=0, top_p=1.0):
+    """Top-k / top-p restricted softmax of one row, token by token from the
+    definition (O(V^2), tiny rows only): v is kept when fewer than k tokens
+    have a larger logit and the mass of the larger-logit tokens is 0 or below
+    top_p times the top-k mass."""
+    l = np.asarray(logits, np.float64)
+    V = l.shape[0]
+    e = np.exp((l - l.max()) / T)
+    use_k = 1 <= top_k < V
+    use_p = not (top_p >= 1.0)
+    in_k = np.array([(not use_k) or int((l > l[v]).sum()) < top_k for v in range(V)])
+    s_k = e[in_k].sum()
+    keep = in_k.copy()
+    if use_p:
+        for v in range(V):
+            a = e[l > l[v]].sum()
+            keep[v] = in_k[v] and (a == 0.0 or a < top_p * s_k)
+    w = np.where(keep, e, 0.0)
+    return w / w.sum()
+
+
 def expected_tokens(alpha: float, gamma: int) -> float:
     """Eq. (1): (1 - alpha^(gamma+1)) / (1 - alpha), limit gamma+1 at alpha = 1."""
     if alpha == 1.0:
@@ -216,3 +237,35 @@ def check_e_layout(tokens, nacc, ids, cu, V):
     assert np.array_equal(tokens[pre], ids[draft_index[pre]])
     tail = off > nacc[req]
     assert np.all(tokens[tail] == -1)
+
+
+def check_adjusted_distribution(run_adj, top_k, top_p, n=400_000, seed=31, T=1.0):
+    """(a) with the adjusted target of the vllbc page's Section 2.2 note: the
+    emitted slot-0 token follows the top-k / top-p restricted p_0, a correction
+    at position 0 follows norm(max(0, p'_0 - q_0)), and a bonus p'_gamma.
+    ``run_adj(tgt, q, ids, cu, T, seed, top_k, top_p)`` returns
+    (tokens, num_accepted, accept, beta)."""
+    rng = np.random.default_rng(seed)
+    V, gamma = 8, 2
+    tgt_rows = np.array([[0.3, -1.0, 1.2, 0.0, 0.7, -0.4, 0.5, -2.0],
+                         [1.0, 0.2, -0.5, 0.9, 0.0, -1.5, 0.4, 0.1],
+                         [-0.2, 0.8, 0.1, -1.0, 1.4, 0.3, -0.6, 0.9]], np.float32)
+    draft_rows = np.array([[0.05, 0.25, 0.10, 0.20, 0.10, 0.15, 0.05, 0.10],
+                           [0.20, 0.15, 0.15, 0.05, 0.20, 0.10, 0.10, 0.05]], np.float32)
+    tgt, q, ids, cu = tile_batch(tgt_rows, draft_rows, n, rng)
+    tokens, nacc, accept, beta = run_adj(tgt, q, ids, cu, T, seed, top_k, top_p)
+    check_e_layout(tokens, nacc, ids, cu, V)
+    tok = tokens.reshape(n, gamma + 1)
+    pa = np.stack([adjusted64(r, T, top_k, top_p) for r in tgt_rows])
+    out = {}
+    out["slot0"] = chi2_ok(np.bincount(tok[:, 0], minlength=V), pa[0])
+    rej0 = nacc == 0
+    resid = np.maximum(pa[0] - draft_rows[0].astype(np.float64), 0.0)
+    out["residual"] = chi2_ok(np.bincount(tok[rej0, 0], minlength=V), resid / resid.sum())
+    full = nacc == gamma
+    out["bonus"] = chi2_ok(np.bincount(tok[full, gamma], minlength=V), pa[gamma])
+    beta0 = np.minimum(pa[0], draft_rows[0].astype(np.float64)).sum()
+    out["beta_err"] = float(np.abs(beta.reshape(n, gamma)[:, 0] - beta0).max())
+    acc0 = accept.reshape(n, gamma)[:, 0].mean()
+    out["accept_z"] = abs(acc0 - beta0) / np.sqrt(beta0 * (1 - beta0) / n)
+    return out
