@@ -53,6 +53,12 @@ def parse_args():
                     default="auto")
     ap.add_argument("--draft", choices=["probs", "onehot"], default="probs",
                     help="onehot: no draft rows (a greedy drafter, q = one-hot at the draft id)")
+    ap.add_argument("--top-k", type=int, default=None,
+                    help="top-k of every request (adjusted target rows)")
+    ap.add_argument("--top-p", type=float, default=None,
+                    help="top-p of every request (adjusted target rows)")
+    ap.add_argument("--adjust-mix", action="store_true",
+                    help="a seeded per-request mix of top-k / top-p settings")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -189,12 +195,14 @@ def recorded_traffic(workload_key: str, kernel: str):
 # CPU oracle timing (baseline / reference arm)
 # ----------------------------------------------------------------------------
 
-def oracle_sample_rate(w, seconds: float, start_request: int = 0):
+def oracle_sample_rate(w, seconds: float, start_request: int = 0, top_k=None, top_p=None):
     """Runs the oracle request by request for about `seconds` of wall time;
     returns (positions/s, requests done, positions done, elapsed)."""
     import oracle
     from speculative_decoding_rejection_decode_gb300.inputs import to_numpy_logits
     cu = w.cu.cpu().numpy().astype("int64")
+    tk = None if top_k is None else top_k.cpu().numpy()
+    tp = None if top_p is None else top_p.cpu().numpy()
     done_req = done_pos = 0
     elapsed = 0.0
     b = start_request
@@ -205,7 +213,9 @@ def oracle_sample_rate(w, seconds: float, start_request: int = 0):
         q = None if w.draft_probs is None else w.draft_probs[d0:d1].cpu().numpy()
         ids = w.draft_ids[d0:d1].cpu().numpy()
         t0 = time.perf_counter()
-        oracle.verify_request(int(b), tgt, q, ids, w.T, w.seed)
+        oracle.verify_request(int(b), tgt, q, ids, w.T, w.seed,
+                              top_k=0 if tk is None else int(tk[b]),
+                              top_p=1.0 if tp is None else float(tp[b]))
         elapsed += time.perf_counter() - t0
         done_req += 1
         done_pos += int(d1 - d0)
@@ -213,9 +223,28 @@ def oracle_sample_rate(w, seconds: float, start_request: int = 0):
     return done_pos / elapsed, done_req, done_pos, elapsed
 
 
+def adjust_settings(w, args, device):
+    """Per-request top-k / top-p tensors for the adjusted-target bench lines
+    (None, None for the plain verify step)."""
+    if args.top_k is None and args.top_p is None and not args.adjust_mix:
+        return None, None
+    from speculative_decoding_rejection_decode_gb300.inputs import make_top_k_top_p
+    if args.adjust_mix:
+        return make_top_k_top_p(w.B, w.V, seed=1000 + args.config, device=device)
+    return make_top_k_top_p(w.B, w.V, seed=0, top_k=args.top_k, top_p=args.top_p, device=device)
+
+
+def adjust_desc(args):
+    if args.adjust_mix:
+        return "seeded per-request mix"
+    if args.top_k is None and args.top_p is None:
+        return None
+    return {"top_k": args.top_k, "top_p": args.top_p}
+
+
 def workload_desc(w, args, flush: bool, in_bytes: int) -> dict:
     gam = w.meta.get("gamma")
-    return {
+    d = {
         "workload": f"{w.name} (standard workload {args.config})",
         "B": w.B, "gamma": list(gam) if isinstance(gam, tuple) else gam, "V": w.V,
         "target_dtype": w.dtype, "draft_dtype": None if w.draft_probs is None else "f32",
@@ -224,6 +253,10 @@ def workload_desc(w, args, flush: bool, in_bytes: int) -> dict:
         "l2": ("flushed between steps (256 MB write)" if flush else
                f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush"),
     }
+    if adjust_desc(args) is not None:
+        d["top_k_top_p"] = adjust_desc(args)
+        d["workload"] += " with top-k / top-p"
+    return d
 
 
 def main():
@@ -255,6 +288,9 @@ def main():
     alg_bytes_step = w.algorithmic_bytes()       # + one extra target row per request
     alg_bytes_rows = tgt_bytes + drf_bytes       # what the row kernel must read
     workload_key = f"config{args.config}-B{w.B}-V{w.V}-{args.path}"
+    tk, tp = adjust_settings(w, args, dev)
+    if tk is not None:
+        workload_key += "-adjusted"
 
     v = sd.Verifier(dev)
     v.reserve(w.n_draft, w.B)
@@ -270,7 +306,7 @@ def main():
 
     def step():
         v(w.target_logits, w.draft_probs, w.draft_ids, w.cu, w.T, w.seed, out=out,
-          request_offset=offset)
+          request_offset=offset, top_k=tk, top_p=tp)
 
     for _ in range(max(3, args.warmup)):
         if flush:
@@ -363,9 +399,9 @@ def main():
         "alpha_mean_beta": float(out.beta.double().mean()),
     }
     if not args.no_e2e:
-        result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset)
+        result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        rate, nreq, npos, el = oracle_sample_rate(w, args.cpu_seconds)
+        rate, nreq, npos, el = oracle_sample_rate(w, args.cpu_seconds, top_k=tk, top_p=tp)
         result["cpu_baseline"] = {
             "value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {nreq} requests ({npos} draft positions) of the same workload, "
@@ -376,7 +412,7 @@ def main():
     dist.close()
 
 
-def measure_e2e(v, w, out, dev, stream, steps, dist, offset):
+def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None):
     """Same metric through the public API with the step's inputs in pinned host
     memory: every step copies them to the device, verifies, and reads the
     tokens, counts and beta back."""
@@ -389,16 +425,23 @@ def measure_e2e(v, w, out, dev, stream, steps, dist, offset):
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         h.copy_(t)
         host[name] = h
+    adj = {}
+    for name, t in (("top_k", tk), ("top_p", tp)):
+        if t is not None:
+            adj[name] = (t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t))
     h_out = {k: torch.empty(getattr(out, k).shape, dtype=getattr(out, k).dtype, pin_memory=True)
              for k in ("tokens", "num_accepted", "beta")}
     h2d = sum(h.numel() * h.element_size() for h in host.values())
+    h2d += sum(h.numel() * h.element_size() for _, h in adj.values())
     d2h = sum(h.numel() * h.element_size() for h in h_out.values())
 
     def one():
         for name, h in host.items():
             getattr(w, name).copy_(h, non_blocking=True)
+        for d, h in adj.values():
+            d.copy_(h, non_blocking=True)
         v(w.target_logits, w.draft_probs, w.draft_ids, w.cu, w.T, w.seed, out=out,
-          request_offset=offset)
+          request_offset=offset, top_k=tk, top_p=tp)
         for k, h in h_out.items():
             h.copy_(getattr(out, k), non_blocking=True)
 
@@ -426,13 +469,17 @@ def run_reference(args, dist):
     from speculative_decoding_rejection_decode_gb300.inputs import make_config
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = make_config(args.config, device=dev, B=args.batch, V=args.vocab)
+    if args.draft == "onehot":
+        w.draft_probs = None
+        w.name += " one-hot drafts"
+    tk, tp = adjust_settings(w, args, "cpu")
     per_step_s = 2.0
     for k in range(args.warmup):
-        oracle_sample_rate(w, 0.0, start_request=k)
+        oracle_sample_rate(w, 0.0, start_request=k, top_k=tk, top_p=tp)
     rates, pos, el = [], 0, 0.0
     t0 = time.perf_counter()
     for k in range(args.steps):
-        r, _, p, e = oracle_sample_rate(w, per_step_s, start_request=k * 7)
+        r, _, p, e = oracle_sample_rate(w, per_step_s, start_request=k * 7, top_k=tk, top_p=tp)
         rates.append(r)
         pos += p
         el += e

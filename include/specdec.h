@@ -40,8 +40,9 @@
  * draft_probs [N_d, V].
  *
  * Ownership: the caller owns every input and output buffer (device memory).  The
- * handle owns a device workspace (per-row softmax statistics, status words and
- * greedy partial keys, 144 bytes per target row, plus 268 bytes per request) and
+ * handle owns a device workspace (per-row softmax statistics, adjusted-row
+ * thresholds, status words and greedy keys, 28 bytes per target row, plus 268
+ * bytes per request) and
  * one stream-ordered error word.  A handle serves one stream at a time; calls on it are
  * asynchronous and never synchronise, except the first call that needs a larger
  * workspace than specdec_reserve() provided (it reads cu[B] back to size it).
@@ -153,6 +154,33 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
                                 int32_t* out_num_accepted, float* out_beta,
                                 float* out_target_prob, float* out_draft_prob,
                                 int32_t* out_accept, void* stream);
+
+/* As specdec_rejection_sample_ex, with the target distribution of every row of
+ * request b restricted by top-k and top-p before the test (the vllbc page's
+ * Section 2.2 note folds top-k and top-p, like temperature, into the adjusted
+ * p that the same rejection test then uses):
+ *   top_k   device [B] int32 or NULL.  top_k[b] in [1, V) keeps the tokens with
+ *           fewer than top_k[b] larger logits (every token tied with the k-th
+ *           largest logit stays); other values switch top-k off for b.
+ *   top_p   device [B] float32 or NULL.  top_p[b] < 1 keeps, among the tokens
+ *           top-k kept, those whose larger-logit tokens hold no mass or less
+ *           than top_p[b] of the top-k mass (the smallest top set reaching
+ *           top_p[b], ties at its edge included); values <= 0 and NaN keep the
+ *           most probable tokens only; values >= 1 switch top-p off for b.
+ * p'_i is then p_i restricted to the kept tokens and renormalised; beta, the
+ * accept test, the correction max(0, p' - q) and the bonus draw all use p'.
+ * Draft probabilities are taken as already adjusted by the caller.  At T == 0
+ * both are ignored (the argmax is always kept).  Adjusted calls run on the
+ * sweep path whatever specdec_set_path asked for; each adjusted row costs a few
+ * extra passes over the row while it is held in L2 (a selection of the
+ * threshold: exact counts, masses as 64-bit fixed point).
+ * NULL, NULL is exactly specdec_rejection_sample_ex. */
+int specdec_rejection_sample_topk_topp(
+    specdec_handle_t h, const void* target_logits, int dtype, const float* draft_probs,
+    const int32_t* draft_ids, const int32_t* cu_num_draft_tokens, int B, int V, float T,
+    const int32_t* top_k, const float* top_p, uint64_t seed, uint64_t request_offset,
+    int32_t* out_tokens, int32_t* out_num_accepted, float* out_beta, float* out_target_prob,
+    float* out_draft_prob, int32_t* out_accept, void* stream);
 
 /* Reads the handle's sticky device error word (SPECDEC_DEVERR_* bits) into
  * *device_error and clears it.  Queues the read on `stream` and waits for it, so

@@ -79,10 +79,12 @@ def _load():
                                                 vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_rejection_sample.restype = i32
         lib.oracle_verify_request_adj.argtypes = [i64, i32, vp, i32, vp, vp, i32, dbl, i32, dbl,
-                                                  u64, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                                  u64, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_verify_request_adj.restype = i32
         lib.oracle_rejection_sample_adj.argtypes = [vp, i32, vp, vp, vp, i32, i32, dbl, vp, vp,
-                                                    u64, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                                    u64, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_pow2_neg.argtypes = [ctypes.c_float]
+        lib.oracle_pow2_neg.restype = ctypes.c_float
         lib.oracle_rejection_sample_adj.restype = i32
         lib.oracle_adjusted_probs.argtypes = [vp, i32, i32, dbl, i32, dbl, vp]
         lib.oracle_adjusted_probs.restype = i32
@@ -137,7 +139,6 @@ class OracleResult:
     pos_near_tie: np.ndarray    # int32 [N_d]
     near_tie: np.ndarray        # int32 [B]
     status: int
-    pos_adj_tie: np.ndarray | None = None   # int32 [N_d] top-p edge near tie in that row
 
 
 def _per_request(a, B: int, dtype, name: str):
@@ -178,14 +179,13 @@ def rejection_sample(target_logits: np.ndarray, draft_probs: np.ndarray | None,
     q_x = np.empty(max(n_d, 1), np.float64)
     acc = np.empty(max(n_d, 1), np.int32)
     pos_tie = np.empty(max(n_d, 1), np.int32)
-    adj_tie = np.empty(max(n_d, 1), np.int32)
     tie = np.empty(B, np.int32)
     st = lib.oracle_rejection_sample_adj(_ptr(logits), dt, _ptr(q), _ptr(ids), _ptr(cu), B, V,
                                          float(T), _ptr(tk), _ptr(tp), seed & 0xFFFFFFFFFFFFFFFF,
                                          _ptr(tokens), _ptr(nacc), _ptr(beta), _ptr(p_x), _ptr(q_x),
-                                         _ptr(acc), _ptr(pos_tie), _ptr(adj_tie), _ptr(tie))
+                                         _ptr(acc), _ptr(pos_tie), _ptr(tie))
     return OracleResult(tokens, nacc, beta[:n_d], p_x[:n_d], q_x[:n_d], acc[:n_d], pos_tie[:n_d],
-                        tie, int(st), adj_tie[:n_d])
+                        tie, int(st))
 
 
 def verify_request(b: int, target_rows: np.ndarray, draft_rows: np.ndarray | None,
@@ -205,20 +205,25 @@ def verify_request(b: int, target_rows: np.ndarray, draft_rows: np.ndarray | Non
     tokens = np.empty(gamma + 1, np.int32)
     nacc = np.empty(1, np.int32)
     beta, p_x, q_x = (np.empty(g1, np.float64) for _ in range(3))
-    acc, pos_tie, adj_tie = (np.empty(g1, np.int32) for _ in range(3))
+    acc, pos_tie = np.empty(g1, np.int32), np.empty(g1, np.int32)
     tie = np.empty(1, np.int32)
     st = lib.oracle_verify_request_adj(b, gamma, _ptr(logits), dt, _ptr(q), _ptr(ids), V, float(T),
                                        int(top_k), float(top_p), seed & 0xFFFFFFFFFFFFFFFF,
                                        _ptr(tokens), _ptr(nacc), _ptr(beta), _ptr(p_x), _ptr(q_x),
-                                       _ptr(acc), _ptr(pos_tie), _ptr(adj_tie), _ptr(tie))
+                                       _ptr(acc), _ptr(pos_tie), _ptr(tie))
     return OracleResult(tokens, nacc, beta[:gamma], p_x[:gamma], q_x[:gamma], acc[:gamma],
-                        pos_tie[:gamma], tie, int(st), adj_tie[:gamma])
+                        pos_tie[:gamma], tie, int(st))
+
+
+def pow2_neg(z: float) -> float:
+    """2^-z on the float32 definition the top-p edge is decided with."""
+    return float(_load().oracle_pow2_neg(float(z)))
 
 
 def adjusted_probs(row: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0,
-                   dtype: str | None = None) -> tuple[np.ndarray, int]:
+                   dtype: str | None = None) -> np.ndarray:
     """The adjusted target distribution of one row of logits (temperature,
-    then top-k, then top-p) and its top-p near-tie flag."""
+    then top-k, then top-p)."""
     lib = _load()
     logits, dt = _logits_array(np.asarray(row).reshape(-1), dtype)
     p = np.empty(logits.shape[0], np.float64)
@@ -226,4 +231,4 @@ def adjusted_probs(row: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0
                                    float(top_p), _ptr(p))
     if st < 0:
         raise ValueError(f"oracle_adjusted_probs failed with status {st}")
-    return p, int(st)
+    return p

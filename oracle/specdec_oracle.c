@@ -58,7 +58,10 @@
  *         smallest top set whose mass reaches P, ties at its edge included);
  *       p'(v) = e(v) / (sum of e over the kept tokens) on the kept tokens, 0
  *         elsewhere.  Draft probabilities are taken as already adjusted.
- *     T == 0 ignores both (the argmax is always kept).
+ *     T == 0 ignores both (the argmax is always kept).  The top-p edge is a
+ *     decision that floating point takes, so it is taken in the precision of
+ *     the CUDA library, on the same numbers (see nucleus_mass below); p' itself
+ *     is computed in double.
  *
  * Counter-based generator (the pages only say "uniform random"): SplitMix64
  * (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
@@ -74,10 +77,7 @@
  * differently from this double-precision one) are flagged per request:
  *   - an accept test with |r - min(1, ratio)| <= 1e-5 * max(r, min(1, ratio))
  *     at a tested position (0..n, or all positions when n == gamma);
- *   - a race whose two best keys k1 >= k2 satisfy k1 - k2 <= 1e-5 * k1;
- *   - a top-p edge with |A - P * S_K| <= 1e-5 * S_K for the last kept or the
- *     first dropped group of equal logits, in a row 0..n (flagged per position
- *     as well, since the whole adjusted row, beta included, depends on it).
+ *   - a race whose two best keys k1 >= k2 satisfy k1 - k2 <= 1e-5 * k1.
  *
  * Parity pins (tests, CPU only): the splitmix64 published output for seed 0,
  * uniformity of U, softmax closed forms, beta by hand on tiny rows and its
@@ -176,11 +176,55 @@ static int by_logit_desc(const void* a, const void* b) {
 }
 
 /*
+ * Masses on which the top-p edge is decided.  The pages fix no precision for
+ * it; the CUDA library takes it in float32, so both sides take it on the same
+ * float32 numbers, each from this written definition:
+ *   c = log2(e) / T and z(v) = (M - L(v)) * c, in float32 (M = max L);
+ *   2^-z = 0 when z >= 64 (or NaN); otherwise 2^-f * 2^-k with k = floor(z),
+ *     f = z - k, and 2^-f the Taylor series sum_{n<=8} (-ln 2)^n f^n / n!
+ *     (coefficients rounded to float32; Horner's rule with fused
+ *     multiply-adds, highest power first);
+ *   the mass of v is the integer round(2^-z * 2^F), F = 62 - ceil(log2 V), so
+ *     that sums over a row are exact and do not depend on their order.
+ * A(v) and S_K of the header comment are sums of these integers and the test
+ * A(v) < P * S_K is evaluated in double as (double)A < (double)P * (double)S_K.
+ * The series is within 4e-7 of 2^-f (relative).
+ */
+static void pow2_neg_coefficients(float* a) {
+  double t = 1.0;
+  for (int n = 0; n <= 8; ++n) {
+    a[n] = (float)t;
+    t *= -log(2.0) / (double)(n + 1);
+  }
+}
+
+static float pow2_neg(float z, const float* a) {
+  if (!(z < 64.0f)) return 0.0f;
+  int k = (int)z;
+  float f = z - (float)k;
+  float q = a[8];
+  for (int n = 7; n >= 0; --n) q = fmaf(q, f, a[n]);
+  return ldexpf(q, -k);
+}
+
+/* Exported for the tests: 2^-z as defined above. */
+float oracle_pow2_neg(float z) {
+  float a[9];
+  pow2_neg_coefficients(a);
+  return pow2_neg(z, a);
+}
+
+static int mass_shift(int V) {
+  int lg = 0;
+  while ((1LL << lg) < (long long)V) ++lg;
+  return 62 - lg;
+}
+
+/*
  * The target distribution of one row after temperature, top-k and top-p (the
  * adjusted p of [P4] Section 2.2; the kept sets are defined in the header
  * comment).  top_k outside [1, V) and top_p >= 1 leave the softmax unchanged.
- * Returns 1 when a top-p decision lies within the near-tie margin, else 0, or
- * ORACLE_OOM.
+ * Returns 0, or ORACLE_OOM.
  */
 static int adjusted_row(const void* logits, int dtype, size_t row, int V, double T, int top_k,
                         double top_p, double* p) {
@@ -203,24 +247,29 @@ static int adjusted_row(const void* logits, int dtype, size_t row, int V, double
     kend = top_k;
     while (kend < V && r[kend].l == r[top_k - 1].l) ++kend;
   }
-  /* S_K: the unnormalised mass e(v) = exp((L(v) - max L) / T) of K */
-  double s_k = 0.0;
-  for (int j = 0; j < kend; ++j) s_k += exp((r[j].l - mx) / T);
-  /* top-p: walk the groups of equal logits inside K */
+  /* top-p: walk the groups of equal logits inside K, on the integer masses */
   int end = kend;
-  int tie = 0;
   if (use_p) {
-    const double bound = top_p * s_k;
-    double above = 0.0;
+    float a[9];
+    pow2_neg_coefficients(a);
+    const int F = mass_shift(V);
+    const float c = 1.4426950408889634f / (float)T;
+    const float m32 = (float)mx;
+    uint64_t s_k = 0;
+    for (int j = 0; j < kend; ++j)
+      s_k += (uint64_t)nearbyintf(ldexpf(pow2_neg((m32 - (float)r[j].l) * c, a), F));
+    const double bound = top_p * (double)s_k;
+    uint64_t above = 0;
     int j = 0;
     end = 0;
     while (j < kend) {
       int g = j;
-      double gm = 0.0;
-      while (g < kend && r[g].l == r[j].l) gm += exp((r[g++].l - mx) / T);
-      const int keep = (above == 0.0) || (above < bound);
-      if ((above > 0.0) && fabs(above - bound) <= NEAR_TIE_REL * s_k) tie = 1;
-      if (!keep) break;
+      uint64_t gm = 0;
+      while (g < kend && r[g].l == r[j].l) {
+        gm += (uint64_t)nearbyintf(ldexpf(pow2_neg((m32 - (float)r[g].l) * c, a), F));
+        ++g;
+      }
+      if (!(above == 0 || (double)above < bound)) break;
       end = g;
       above += gm;
       j = g;
@@ -232,7 +281,7 @@ static int adjusted_row(const void* logits, int dtype, size_t row, int V, double
   for (int j = end; j < V; ++j) p[r[j].v] = 0.0;
   for (int j = 0; j < end; ++j) p[r[j].v] = exp((r[j].l - mx) / T) / kept;
   free(r);
-  return tie;
+  return 0;
 }
 
 /* Exported for the tests: the adjusted distribution of one row of V logits. */
@@ -275,9 +324,7 @@ static int argmax_row(const void* logits, int dtype, size_t row, int V) {
  *   accept [gamma]    the accept test at every position (also after the first
  *                     rejection, where it no longer affects the output)
  *   pos_near_tie [gamma]  accept-test near tie at that position
- *   pos_adj_tie [gamma]   top-p near tie in that position's target row
- *   near_tie [1]      request-level flag (tested positions, their top-p edges,
- *                     the extra token's row or the race)
+ *   near_tie [1]      request-level flag (tested positions or the race)
  * top_k / top_p adjust every target row of the request (top_k outside [1, V)
  * and top_p >= 1 switch them off; T == 0 ignores them).
  * Returns ORACLE_OK, ORACLE_BAD_DRAFT_ID or ORACLE_OOM.
@@ -286,7 +333,7 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
                               const float* draft, const int32_t* ids, int V, double T, int top_k,
                               double top_p, uint64_t seed, int32_t* tokens, int32_t* num_accepted,
                               double* beta, double* p_x, double* q_x, int32_t* accept,
-                              int32_t* pos_near_tie, int32_t* pos_adj_tie, int32_t* near_tie) {
+                              int32_t* pos_near_tie, int32_t* near_tie) {
   int status = ORACLE_OK;
   int n = gamma;
   int req_tie = 0;
@@ -324,8 +371,6 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
       }
     t = g[n];
     free(g);
-    if (pos_adj_tie)
-      for (int i = 0; i < gamma; ++i) pos_adj_tie[i] = 0;
   } else {
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     if (!p) {
@@ -348,19 +393,9 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
       draft = onehot;
     }
     /* Accept test and beta at every draft position. */
-    int* atie = (int*)calloc((size_t)(gamma + 1), sizeof(int));
-    if (!atie) {
-      free(onehot);
-      free(p);
-      free(acc);
-      free(tie);
-      return ORACLE_OOM;
-    }
     for (int i = 0; i < gamma; ++i) {
       const float* q = draft + (size_t)i * (size_t)V;
-      atie[i] = adjusted_row(tgt, dtype, (size_t)i, V, T, top_k, top_p, p);
-      if (atie[i] == ORACLE_OOM) {
-        free(atie);
+      if (adjusted_row(tgt, dtype, (size_t)i, V, T, top_k, top_p, p) == ORACLE_OOM) {
         free(onehot);
         free(p);
         free(acc);
@@ -398,29 +433,25 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
         n = i;
         break;
       }
-    for (int i = 0; i < gamma && i <= n; ++i) req_tie |= tie[i] | atie[i];
+    for (int i = 0; i < gamma && i <= n; ++i) req_tie |= tie[i];
 
     /* Correction (n < gamma) or bonus (n == gamma) distribution w. */
     double* w = (double*)malloc(sizeof(double) * (size_t)V);
     if (!w) {
-      free(atie);
       free(onehot);
       free(p);
       free(acc);
       free(tie);
       return ORACLE_OOM;
     }
-    atie[gamma] = adjusted_row(tgt, dtype, (size_t)n, V, T, top_k, top_p, p);
-    if (atie[gamma] == ORACLE_OOM) {
+    if (adjusted_row(tgt, dtype, (size_t)n, V, T, top_k, top_p, p) == ORACLE_OOM) {
       free(w);
-      free(atie);
       free(onehot);
       free(p);
       free(acc);
       free(tie);
       return ORACLE_OOM;
     }
-    req_tie |= atie[gamma];
     if (n < gamma) {
       const float* q = draft + (size_t)n * (size_t)V;
       int any = 0;
@@ -450,9 +481,6 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
       }
     }
     if (k2 > -INFINITY && (k1 - k2) <= NEAR_TIE_REL * k1) req_tie = 1;
-    if (pos_adj_tie)
-      for (int i = 0; i < gamma; ++i) pos_adj_tie[i] = atie[i];
-    free(atie);
     free(w);
     free(p);
     free(onehot);
@@ -480,8 +508,7 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
                           int32_t* num_accepted, double* beta, double* p_x, double* q_x,
                           int32_t* accept, int32_t* pos_near_tie, int32_t* near_tie) {
   return oracle_verify_request_adj(b, gamma, tgt, dtype, draft, ids, V, T, 0, 1.0, seed, tokens,
-                                   num_accepted, beta, p_x, q_x, accept, pos_near_tie, NULL,
-                                   near_tie);
+                                   num_accepted, beta, p_x, q_x, accept, pos_near_tie, near_tie);
 }
 
 /* ---------------------------------------------------------------------- */
@@ -500,8 +527,7 @@ int oracle_rejection_sample_adj(const void* target_logits, int dtype, const floa
                                 const int32_t* top_k, const double* top_p, uint64_t seed,
                                 int32_t* out_tokens, int32_t* out_num_accepted, double* out_beta,
                                 double* out_p_x, double* out_q_x, int32_t* out_accept,
-                                int32_t* out_pos_near_tie, int32_t* out_pos_adj_tie,
-                                int32_t* out_near_tie) {
+                                int32_t* out_pos_near_tie, int32_t* out_near_tie) {
   if (B <= 0 || V <= 0 || !target_logits || !draft_ids || !cu) return ORACLE_INVALID_ARG;
   if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
   if (!(T >= 0.0) || isinf(T)) return ORACLE_INVALID_ARG;
@@ -522,7 +548,7 @@ int oracle_rejection_sample_adj(const void* target_logits, int dtype, const floa
         out_num_accepted ? out_num_accepted + b : NULL, out_beta ? out_beta + d0 : NULL,
         out_p_x ? out_p_x + d0 : NULL, out_q_x ? out_q_x + d0 : NULL,
         out_accept ? out_accept + d0 : NULL, out_pos_near_tie ? out_pos_near_tie + d0 : NULL,
-        out_pos_adj_tie ? out_pos_adj_tie + d0 : NULL, out_near_tie ? out_near_tie + b : NULL);
+        out_near_tie ? out_near_tie + b : NULL);
     if (s == ORACLE_OOM) return s;
     if (s != ORACLE_OK) status = s;
   }
@@ -537,5 +563,5 @@ int oracle_rejection_sample(const void* target_logits, int dtype, const float* d
                             int32_t* out_pos_near_tie, int32_t* out_near_tie) {
   return oracle_rejection_sample_adj(target_logits, dtype, draft_probs, draft_ids, cu, B, V, T, NULL,
                                      NULL, seed, out_tokens, out_num_accepted, out_beta, out_p_x,
-                                     out_q_x, out_accept, out_pos_near_tie, NULL, out_near_tie);
+                                     out_q_x, out_accept, out_pos_near_tie, out_near_tie);
 }

@@ -64,6 +64,8 @@ _rs = _fn("specdec_rejection_sample", _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32,
           _vp, _vp, _vp, _vp)
 _rs_ex = _fn("specdec_rejection_sample_ex", _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _f32,
              _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
+_rs_adj = _fn("specdec_rejection_sample_topk_topp", _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32,
+              _i32, _f32, _vp, _vp, _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _get_error = _fn("specdec_get_error", _i32, _vp, ctypes.POINTER(_i32), _vp)
 _set_path = _fn("specdec_set_path", _i32, _vp, _i32)
 _set_events = _fn("specdec_set_timing_events", _i32, _vp, _vp, _vp)
@@ -99,6 +101,15 @@ def specdec_rejection_sample_ex(h, target_logits, dtype, draft_probs, draft_ids,
     return _rs_ex(h, target_logits, dtype, draft_probs, draft_ids, cu_num_draft_tokens, B, V, T,
                   seed & 0xFFFFFFFFFFFFFFFF, request_offset, out_tokens, out_num_accepted,
                   out_beta, out_target_prob, out_draft_prob, out_accept, stream)
+
+
+def specdec_rejection_sample_topk_topp(h, target_logits, dtype, draft_probs, draft_ids,
+                                       cu_num_draft_tokens, B, V, T, top_k, top_p, seed,
+                                       request_offset, out_tokens, out_num_accepted, out_beta,
+                                       out_target_prob, out_draft_prob, out_accept, stream) -> int:
+    return _rs_adj(h, target_logits, dtype, draft_probs, draft_ids, cu_num_draft_tokens, B, V, T,
+                   top_k, top_p, seed & 0xFFFFFFFFFFFFFFFF, request_offset, out_tokens,
+                   out_num_accepted, out_beta, out_target_prob, out_draft_prob, out_accept, stream)
 
 
 def specdec_set_timing_events(h: int, before_rows, after_rows) -> int:
@@ -147,7 +158,8 @@ def specdec_destroy(h: int) -> int:
 
 
 EXPORTED = ["specdec_create", "specdec_reserve", "specdec_rejection_sample",
-            "specdec_rejection_sample_ex", "specdec_get_error", "specdec_set_path",
+            "specdec_rejection_sample_ex", "specdec_rejection_sample_topk_topp",
+            "specdec_get_error", "specdec_set_path",
             "specdec_set_timing_events",
             "specdec_last_path", "specdec_uniform", "specdec_neg_log_uniform",
             "specdec_rejection_sample_noalloc", "specdec_status_string", "specdec_destroy"]

@@ -25,6 +25,8 @@
 // Non-template kernels are `static`: each translation unit that launches them
 // (the handle path and the allocation-free path) keeps its own copy.
 
+#include <type_traits>
+
 #include "device_common.cuh"
 
 namespace specdec {
@@ -61,6 +63,9 @@ struct Params {
   int rslices;             // slices per deferred row
   int rslice_len;          // elements per slice (multiple of 8)
   unsigned long long* sched;  // [1] next work slot of the sweep kernel (reset by finalize)
+  const int32_t* topk;     // [B] per-request top-k or null (adjusted rows, sweep kernel only)
+  const float* topp;       // [B] per-request top-p or null
+  float* row_tau;          // [cap_rows] logit threshold of each adjusted row, or null
   uint32_t* err;           // [1] sticky device error word
   int64_t cap_rows;
   int cap_b;
@@ -464,15 +469,20 @@ __device__ __forceinline__ void softmax_acc16(const uint4& w, float& m, float& s
   }
 }
 
-// Sweep-2 work on 4 consecutive vocabulary entries starting at v.
-template <bool kHasQ, bool kRace>
+// Sweep-2 work on 4 consecutive vocabulary entries starting at v.  With kMask
+// the entries below tau are outside the adjusted row (p = 0).
+template <bool kHasQ, bool kRace, bool kMask>
 __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float M, float c,
-                                         float invS, bool resid, uint64_t rkey, uint32_t v,
-                                         float& beta, Race& best, int excl = -1) {
+                                         float invS, float tau, bool resid, uint64_t rkey,
+                                         uint32_t v, float& beta, Race& best, int excl = -1) {
   const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
   float p[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) p[k] = ex2((l[k] - M) * c) * invS;
+  if constexpr (kMask) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) p[k] = l[k] >= tau ? p[k] : 0.0f;
+  }
   if constexpr (kHasQ)
     beta += (fminf(p[0], qv[0]) + fminf(p[1], qv[1])) + (fminf(p[2], qv[2]) + fminf(p[3], qv[3]));
   if constexpr (kRace) {
@@ -493,10 +503,11 @@ __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float
 
 // Sweep 2 over vectors [lo, hi) of the row (elements [lo, hi) when the row is
 // not 16-byte aligned).
-template <typename TT, int NT, bool kHasQ, bool kRace>
+template <typename TT, int NT, bool kHasQ, bool kRace, bool kMask = false>
 __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo, int hi, bool vec,
-                                       float M, float c, float invS, bool resid, uint64_t rkey,
-                                       uint64_t pol, float& beta, Race& best, int excl = -1) {
+                                       float M, float c, float invS, float tau, bool resid,
+                                       uint64_t rkey, uint64_t pol, float& beta, Race& best,
+                                       int excl = -1) {
   constexpr int kEl = 16 / sizeof(TT);
   // target vectors loaded per iteration: fewer where the race needs registers
   constexpr int U = kRace ? 2 : (sizeof(TT) == 2 ? 3 : 4);
@@ -526,8 +537,8 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
         for (int h = 0; h < kEl / 4; ++h) {
           float4 q4 = zero4;
           if constexpr (kHasQ) q4 = *reinterpret_cast<const float4*>(&b[u][h]);
-          sweep2_4<kHasQ, kRace>(x + 4 * h, q4, M, c, invS, resid, rkey,
-                                 (uint32_t)((j + u * NT) * kEl + 4 * h), beta, best, excl);
+          sweep2_4<kHasQ, kRace, kMask>(x + 4 * h, q4, M, c, invS, tau, resid, rkey,
+                                        (uint32_t)((j + u * NT) * kEl + 4 * h), beta, best, excl);
         }
       }
     }
@@ -541,13 +552,15 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
           uint4 w = ldg_hint(qv + j * (kEl / 4) + h, pol);
           q4 = *reinterpret_cast<const float4*>(&w);
         }
-        sweep2_4<kHasQ, kRace>(x + 4 * h, q4, M, c, invS, resid, rkey, (uint32_t)(j * kEl + 4 * h),
-                               beta, best, excl);
+        sweep2_4<kHasQ, kRace, kMask>(x + 4 * h, q4, M, c, invS, tau, resid, rkey,
+                                      (uint32_t)(j * kEl + 4 * h), beta, best, excl);
       }
     }
   } else {
     for (int v = lo + tid; v < hi; v += NT) {
-      const float p = ex2((load_logit(row + v) - M) * c) * invS;
+      const float xv = load_logit(row + v);
+      float p = ex2((xv - M) * c) * invS;
+      if constexpr (kMask) p = xv >= tau ? p : 0.0f;
       float qv = 0.0f;
       if constexpr (kHasQ) {
         qv = __ldg(qrow + v);
@@ -596,11 +609,315 @@ __device__ __forceinline__ void sweep1(const TT* row, int lo, int hi, bool vec, 
   s = s0;
 }
 
-template <typename TT, int NT, int MINB>
+// ---------------------------------------------------------------------------
+// Top-k / top-p adjusted target rows (the vllbc page's Section 2.2 note: top-k
+// and top-p fold into the adjusted p before the same rejection test).
+//
+// Kept set of a row with e(v) = exp2((l_v - M) c):
+//   top-k (1 <= k < V): v with fewer than k logits above l_v (ties at the k-th
+//                       largest logit all stay);
+//   top-p (P < 1):      v with A(v) = 0 or A(v) < P * S_k, A(v) the mass of the
+//                       logits above l_v and S_k the mass kept by top-k.
+// Both are a threshold on the logit: the kept set is {v : l_v >= tau}.  tau is
+// found by a selection over the row while it is still in L2: a first pass
+// bins every entry by z = (M - l) c (64 bins per unit of z, so the bins are
+// linear in the logit near the top of the row, where the edge usually falls;
+// z >= 32 shares the last bin), then each further pass splits the chosen bin
+// into 1024 sub-bins, by finer z first and by the order-preserving 32-bit key
+// of the logit after that, until the chosen sub-bin holds a single logit
+// value.  Counts are exact; masses are integers (pow2_neg(z) scaled by 2^F
+// with V 2^F <= 2^62), so the shared-memory histograms add up the same way in
+// any order, the result does not depend on thread timing, and the top-p test
+// (double)A < (double)P * (double)S_k sees the numbers a CPU restatement sees.
+// ---------------------------------------------------------------------------
+constexpr int kAdjBins1 = 2048;
+constexpr int kAdjBins2 = 1024;
+constexpr float kAdjZ1 = 64.0f;          // level-1 bins per unit of z
+constexpr float kAdjZ2 = 65536.0f;       // level-2 sub-bins per unit of z (kAdjZ1 * kAdjBins2)
+constexpr int kAdjMaxKeyLevels = 4;      // 1024^4 > 2^32: key levels always end on one value
+
+struct AdjShared {
+  uint32_t cnt1[kAdjBins1];
+  unsigned long long mass1[kAdjBins1];
+  uint32_t cnt2[kAdjBins2];
+  unsigned long long mass2[kAdjBins2];
+  uint32_t kmin2[kAdjBins2];
+  uint32_t kmax2[kAdjBins2];
+  uint32_t wcnt[32];
+  unsigned long long wmass[32];
+  int sel;
+  uint32_t ex_cnt;
+  unsigned long long ex_mass;
+};
+
+// Mass of an entry for the selection: 2^-z on a float32 definition that a CPU
+// implementation can reproduce bit for bit, so that the top-p edge (a decision
+// floating point takes) comes out the same on both: 0 for z >= 64 (or NaN);
+// otherwise 2^-f * 2^-k with k = floor(z), f = z - k, and 2^-f the Taylor
+// series of degree 8, coefficients (-ln 2)^n / n! rounded to float32, by
+// Horner's rule with fused multiply-adds.  Within 4e-7 of 2^-z.
+__device__ __forceinline__ float pow2_neg(float z) {
+  if (!(z < 64.0f)) return 0.0f;
+  const int k = (int)z;
+  const float f = z - (float)k;
+  float q = 1.3215486790144305e-06f;
+  q = __fmaf_rn(q, f, -1.5252733804059838e-05f);
+  q = __fmaf_rn(q, f, 0.00015403530393381606f);
+  q = __fmaf_rn(q, f, -0.0013333558146428441f);
+  q = __fmaf_rn(q, f, 0.009618129107628477f);
+  q = __fmaf_rn(q, f, -0.055504108664821576f);
+  q = __fmaf_rn(q, f, 0.2402265069591007f);
+  q = __fmaf_rn(q, f, -0.6931471805599453f);
+  q = __fmaf_rn(q, f, 1.0f);
+  return q * __int_as_float((127 - k) << 23);  // exact: q >= 1/2, k <= 63
+}
+
+// Order-preserving key of a logit (-0.0 folded into +0.0).
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One histogram pass over the row.
+//   mode 1: every entry into the level-1 bins (count, and mass when need_mass);
+//   mode 2: entries of level-1 bin j1 (< last) into sub-bins of z / 65536;
+//   mode 3: entries with key in [lo, hi] (and, when j1 >= 0, in level-1 bin j1)
+//           into sub-bins of `w` consecutive keys, counted down from hi.
+// At every level bin 0 holds the largest logits.
+// Modes 2 and 3 also keep each sub-bin's smallest and largest key.
+template <typename TT, int NT>
+__device__ __forceinline__ void adj_pass(const TT* row, int V, bool vec, float M, float c,
+                                         float fscale, int mode, bool need_mass, int j1,
+                                         uint32_t lo, uint32_t hi, uint32_t w, uint64_t pol,
+                                         AdjShared& A) {
+  constexpr int kEl = 16 / sizeof(TT);
+  auto add = [&](float x) {
+    const float z = (M - x) * c;
+    const float y = z * kAdjZ1;
+    const int b1 = y < (float)(kAdjBins1 - 1) ? (int)y : kAdjBins1 - 1;
+    if (mode == 1) {
+      atomicAdd(&A.cnt1[b1], 1u);
+      if (need_mass) atomicAdd(&A.mass1[b1], __float2ull_rn(pow2_neg(z) * fscale));
+      return;
+    }
+    int s;
+    uint32_t k = order_key(x);
+    if (mode == 2) {
+      if (b1 != j1) return;
+      s = (int)(z * kAdjZ2) - j1 * kAdjBins2;
+    } else {
+      if (k < lo || k > hi || (j1 >= 0 && b1 != j1)) return;
+      s = (int)((hi - k) / w);  // sub-bin 0 holds the largest keys, like every other level
+    }
+    if ((unsigned)s >= (unsigned)kAdjBins2) return;  // cannot happen for the bins chosen above
+    atomicAdd(&A.cnt2[s], 1u);
+    atomicAdd(&A.mass2[s], __float2ull_rn(pow2_neg(z) * fscale));
+    atomicMin(&A.kmin2[s], k);
+    atomicMax(&A.kmax2[s], k);
+  };
+  const int tid = threadIdx.x;
+  if (vec) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    const int nv = V / kEl;
+    int j = tid;
+    for (; j + 3 * NT < nv; j += 4 * NT) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = ldg_hint(rv + j + u * NT, pol);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float x[kEl];
+        unpack16<TT>(a[u], x);
+#pragma unroll
+        for (int e = 0; e < kEl; ++e) add(x[e]);
+      }
+    }
+    for (; j < nv; j += NT) {
+      float x[kEl];
+      unpack16<TT>(ldg_hint(rv + j, pol), x);
+#pragma unroll
+      for (int e = 0; e < kEl; ++e) add(x[e]);
+    }
+  } else {
+    for (int v = tid; v < V; v += NT) add(load_logit(row + v));
+  }
+}
+
+// First bin j of [0, n) (bins run from the largest logits down) at which
+//   by count: the running count through j reaches `need`;
+//   by mass:  cnt[j] > 0 and above + the running mass through j >= bound.
+// Leaves j in A.sel (n when no bin qualifies) and the count and mass of the
+// bins before it in A.ex_cnt / A.ex_mass.  Block-wide; ends on a barrier.
+template <int NT>
+__device__ __forceinline__ void adj_select(const uint32_t* cnt, const unsigned long long* mass,
+                                           int n, bool by_mass, uint32_t need, double bound,
+                                           unsigned long long above, AdjShared& A) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = n / NT;
+  const int j0 = tid * per;
+  uint32_t lc = 0;
+  unsigned long long lm = 0;
+  for (int q = 0; q < per; ++q) {
+    lc += cnt[j0 + q];
+    lm += mass[j0 + q];
+  }
+  uint32_t ic = lc;
+  unsigned long long im = lm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t c2 = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+    const unsigned long long m2 = __shfl_up_sync(0xFFFFFFFFu, im, o);
+    if (lane >= o) {
+      ic += c2;
+      im += m2;
+    }
+  }
+  if (lane == 31) {
+    A.wcnt[warp] = ic;
+    A.wmass[warp] = im;
+  }
+  if (tid == 0) A.sel = n;
+  __syncthreads();
+  uint32_t ec = ic - lc;
+  unsigned long long em = im - lm;
+  for (int w = 0; w < warp; ++w) {
+    ec += A.wcnt[w];
+    em += A.wmass[w];
+  }
+  uint32_t rc = ec;
+  unsigned long long rm = em;
+  int found = -1;
+  for (int q = 0; q < per; ++q) {
+    const int j = j0 + q;
+    rc += cnt[j];
+    rm += mass[j];
+    const bool ok = by_mass ? (cnt[j] > 0 && (double)(above + rm) >= bound) : (rc >= need);
+    if (ok) {
+      found = j;
+      break;
+    }
+  }
+  if (found >= 0) atomicMin(&A.sel, found);
+  __syncthreads();
+  const int sel = A.sel;
+  if (sel < n && sel >= j0 && sel < j0 + per) {
+    for (int j = j0; j < sel; ++j) {
+      ec += cnt[j];
+      em += mass[j];
+    }
+    A.ex_cnt = ec;
+    A.ex_mass = em;
+  }
+  __syncthreads();
+}
+
+// Refines the level-1 histogram down to the single logit value at which the
+// criterion (see adj_select) is met.  Returns its key and the mass of every
+// entry whose key is >= it; false when no bin qualifies (rows holding NaN).
+template <typename TT, int NT>
+__device__ bool adj_resolve(const TT* row, int V, bool vec, float M, float c, float fscale,
+                            bool by_mass, uint32_t need, double bound, uint64_t pol, AdjShared& A,
+                            uint32_t& key, unsigned long long& kept) {
+  const int tid = threadIdx.x;
+  adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, need, bound, 0ull, A);
+  const int j1 = A.sel;
+  uint32_t above_c = A.ex_cnt;
+  unsigned long long above_m = A.ex_mass;
+  __syncthreads();
+  if (j1 >= kAdjBins1) return false;
+  // level 2: finer z inside a regular bin; keys below the max for the last bin
+  int mode = j1 < kAdjBins1 - 1 ? 2 : 3;
+  int zf = j1;
+  uint32_t lo = 0, hi = order_key(M);
+  uint32_t w = (uint32_t)(((unsigned long long)hi - lo + kAdjBins2) / kAdjBins2);
+  for (int level = 0; level <= kAdjMaxKeyLevels; ++level) {
+    for (int j = tid; j < kAdjBins2; j += NT) {
+      A.cnt2[j] = 0u;
+      A.mass2[j] = 0ull;
+      A.kmin2[j] = 0xFFFFFFFFu;
+      A.kmax2[j] = 0u;
+    }
+    __syncthreads();
+    adj_pass<TT, NT>(row, V, vec, M, c, fscale, mode, true, zf, lo, hi, w, pol, A);
+    __syncthreads();
+    adj_select<NT>(A.cnt2, A.mass2, kAdjBins2, by_mass, need - above_c, bound, above_m, A);
+    const int s = A.sel;
+    bool done = false;
+    if (s < kAdjBins2) {
+      above_c += A.ex_cnt;
+      above_m += A.ex_mass;
+      lo = A.kmin2[s];
+      hi = A.kmax2[s];
+      done = lo == hi;
+      if (done) {
+        key = lo;
+        kept = above_m + A.mass2[s];
+      }
+    }
+    __syncthreads();
+    if (s >= kAdjBins2 || lo > hi) return false;
+    if (done) return true;
+    mode = 3;
+    zf = -1;
+    w = (uint32_t)(((unsigned long long)hi - lo + kAdjBins2) / kAdjBins2);
+  }
+  return false;
+}
+
+// Threshold tau (keep l >= tau) and kept mass S of an adjusted row whose max is
+// M.  Block-wide (every thread of the block calls it with the same arguments).
+// Returns false, leaving tau and S alone, when no threshold exists (NaN rows).
+template <typename TT, int NT>
+__device__ bool adjust_row(const TT* row, int V, bool vec, float M, float c, int top_k,
+                           float top_p, bool use_k, bool use_p, uint64_t pol, AdjShared& A,
+                           float& tau, float& S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // masses are e * 2^F with V * 2^F <= 2^62
+  const int lg = V > 1 ? 32 - __clz(V - 1) : 0;
+  const int F = 62 - lg;
+  const float fscale = __int_as_float((127 + F) << 23);
+  const double unscale = __longlong_as_double((long long)(1023 - F) << 52);
+  for (int j = tid; j < kAdjBins1; j += NT) {
+    A.cnt1[j] = 0u;
+    A.mass1[j] = 0ull;
+  }
+  __syncthreads();
+  adj_pass<TT, NT>(row, V, vec, M, c, fscale, 1, true, 0, 0u, 0u, 1u, pol, A);
+  __syncthreads();
+  unsigned long long tm = 0;
+  for (int j = tid; j < kAdjBins1; j += NT) tm += A.mass1[j];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tm += __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+  if (lane == 0) A.wmass[warp] = tm;
+  __syncthreads();
+  unsigned long long kept = 0;
+  for (int w = 0; w < NT / 32; ++w) kept += A.wmass[w];
+  __syncthreads();
+  uint32_t key = 0u;  // below every logit
+  if (use_k && !adj_resolve<TT, NT>(row, V, vec, M, c, fscale, false, (uint32_t)top_k, 0.0, pol,
+                                    A, key, kept))
+    return false;
+  if (use_p) {
+    const double bound = (top_p > 0.0f ? (double)top_p : 0.0) * (double)kept;
+    if (!adj_resolve<TT, NT>(row, V, vec, M, c, fscale, true, 0u, bound, pol, A, key, kept))
+      return false;
+  }
+  tau = key_value(key);
+  S = (float)((double)kept * unscale);
+  return true;
+}
+
+// kAdj: requests may carry top-k / top-p (P.topk, P.topp); their rows get a
+// threshold tau and the kept mass as S before sweep 2.
+template <typename TT, int NT, int MINB, bool kAdj = false>
 __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
   constexpr int NW = NT / 32;
   constexpr int kEl = 16 / sizeof(TT);
   __shared__ float4 red[2][NW];
+  __shared__ std::conditional_t<kAdj, AdjShared, char> adj;
   __shared__ long long s_slot;
   __shared__ int s_gmax, s_bad, s_prefix, s_x;
   __shared__ float s_dec[4];  // px, qx, flags
@@ -691,6 +1008,14 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     __syncthreads();
     float M = -INFINITY, S = 0.0f;
     for (int w = 0; w < NW; ++w) softmax_merge(M, S, red[par][w].x, red[par][w].y, P.c);
+    float tau = -INFINITY;
+    if constexpr (kAdj) {
+      const int kk = P.topk ? __ldg(P.topk + b) : 0;
+      const float pp = P.topp ? __ldg(P.topp + b) : 1.0f;
+      const bool use_k = kk >= 1 && kk < V, use_p = !(pp >= 1.0f);
+      if ((use_k || use_p) && M > -INFINITY && M < INFINITY)
+        adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, keep, adj, tau, S);
+    }
     const float invS = 1.0f / S;
 
     // ---- accept test (thread 0) and the race decision --------------------
@@ -698,7 +1023,7 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
       float px = 0.0f;
       bool acc = false;
       if (has_q) {
-        if (valid) px = ex2((lx - M) * P.c) * invS;
+        if (valid && lx >= tau) px = ex2((lx - M) * P.c) * invS;
         const float r = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
         acc = accept_test(r, px, qx);
       }
@@ -721,12 +1046,14 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     float beta = 0.0f;
     Race best = race_none();
     if (has_q && !onehot && race)
-      sweep2<TT, NT, true, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, true, true, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
+                                       beta, best);
     else if (has_q && !onehot)
-      sweep2<TT, NT, true, false>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, true, false, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
+                                        beta, best);
     else if (race)
-      sweep2<TT, NT, false, true>(row, qrow, 0, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best,
-                                  resid ? s_x : -1);
+      sweep2<TT, NT, false, true, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
+                                        beta, best, resid ? s_x : -1);
     beta = warp_sum(beta);
     warp_race(best);
     if (lane == 0) red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
@@ -740,6 +1067,7 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
         race_merge(tb, r4.y, r4.z, __float_as_int(r4.w));
       }
       P.row_stats[t] = make_float2(M, S);
+      if (kAdj && P.row_tau) P.row_tau[t] = tau;
       uint32_t st = kStDone;
       if (has_q) {
         if (flags & 4) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
@@ -942,11 +1270,14 @@ __global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
     float beta = 0.0f;
     Race best = race_none();
     if (has_q && race)
-      sweep2<TT, NT, true, true>(row, qrow, lo, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, true, true>(row, qrow, lo, hi, vec, M, P.c, invS, -INFINITY, resid, rkey, drop,
+                                 beta, best);
     else if (has_q)
-      sweep2<TT, NT, true, false>(row, qrow, lo, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, true, false>(row, qrow, lo, hi, vec, M, P.c, invS, -INFINITY, resid, rkey, drop,
+                                  beta, best);
     else if (race)
-      sweep2<TT, NT, false, true>(row, qrow, lo, hi, vec, M, P.c, invS, resid, rkey, drop, beta, best);
+      sweep2<TT, NT, false, true>(row, qrow, lo, hi, vec, M, P.c, invS, -INFINITY, resid, rkey, drop,
+                                  beta, best);
     beta = warp_sum(beta);
     warp_race(best);
     if (lane == 0) S.red[1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
@@ -1260,11 +1591,11 @@ __global__ void __launch_bounds__(kStreamThreads, MINB) stream_row_kernel(const 
             q4 = reinterpret_cast<const float4*>(ring + (size_t)st_q[e4 >> 10] * kStageBytes)[e4 & 1023];
           const uint32_t v = (uint32_t)(c * kEl1 + 4 * e4);
           if (has_q && race)
-            sweep2_4<true, true>(l, q4, M, P.c, invS, resid, rkey, v, beta, best);
+            sweep2_4<true, true, false>(l, q4, M, P.c, invS, -INFINITY, resid, rkey, v, beta, best);
           else if (has_q)
-            sweep2_4<true, false>(l, q4, M, P.c, invS, resid, rkey, v, beta, best);
+            sweep2_4<true, false, false>(l, q4, M, P.c, invS, -INFINITY, resid, rkey, v, beta, best);
           else
-            sweep2_4<false, true>(l, q4, M, P.c, invS, resid, rkey, v, beta, best);
+            sweep2_4<false, true, false>(l, q4, M, P.c, invS, -INFINITY, resid, rkey, v, beta, best);
         }
       }
       __syncwarp();
@@ -1475,6 +1806,7 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
     const bool has_q = n < g;
     const float2 ms = P.row_stats[t];
     const float invS = 1.0f / ms.y;
+    const float tau = P.row_tau ? P.row_tau[t] : -INFINITY;  // adjusted rows keep l >= tau
     const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
     const bool onehot = P.q == nullptr;
     const float* qrow = (has_q && !onehot) ? P.q + ((int64_t)c0 + n) * (int64_t)V : nullptr;
@@ -1483,7 +1815,8 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
     const int v0 = sl * P.rslice_len, v1 = min(V, v0 + P.rslice_len);
     Race best = race_none();
     for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-      const float p = ex2((load_logit(row + v) - ms.x) * P.c) * invS;
+      const float xv = load_logit(row + v);
+      const float p = xv >= tau ? ex2((xv - ms.x) * P.c) * invS : 0.0f;
       const float w = qrow ? fmaxf(p - __ldg(qrow + v), 0.0f) : (v == excl ? 0.0f : p);
       race_offer(best, w, rkey, (uint32_t)v);
     }
@@ -1503,8 +1836,10 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
       }
       if (!(all.w > 0.0f)) {  // empty residual: race over p instead
         Race bp = race_none();
-        for (int v = threadIdx.x; v < V; v += blockDim.x)
-          race_offer(bp, ex2((load_logit(row + v) - ms.x) * P.c) * invS, rkey, (uint32_t)v);
+        for (int v = threadIdx.x; v < V; v += blockDim.x) {
+          const float xv = load_logit(row + v);
+          race_offer(bp, xv >= tau ? ex2((xv - ms.x) * P.c) * invS : 0.0f, rkey, (uint32_t)v);
+        }
         all = block_race<TT>(bp, red);
       }
       if (threadIdx.x == 0) {

@@ -22,6 +22,7 @@ struct Workspace {
   int64_t cap_rows = 0;
   int cap_b = 0;
   float2* row_stats = nullptr;
+  float* row_tau = nullptr;
   uint64_t* status = nullptr;
   uint64_t* gkeys = nullptr;
   int32_t* ws_nacc = nullptr;
@@ -75,13 +76,14 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   rows = std::max<int64_t>(rows, 1);
   b = std::max(b, 1);
   const size_t stats_b = round_up(rows * sizeof(float2), 256);
+  const size_t tau_b = round_up(rows * sizeof(float), 256);
   const size_t status_b = round_up(rows * sizeof(uint64_t), 256);
   const size_t gkeys_b = round_up(rows * sizeof(uint64_t), 256);
   const size_t nacc_b = round_up((size_t)b * sizeof(int32_t), 256);
   const size_t list_b = nacc_b;
   const size_t rpart_b = round_up((size_t)b * kRaceMaxSlices * sizeof(float4), 256);
   const size_t rcount_b = nacc_b;
-  const size_t total = stats_b + status_b + gkeys_b + nacc_b + list_b + rpart_b + rcount_b;
+  const size_t total = stats_b + tau_b + status_b + gkeys_b + nacc_b + list_b + rpart_b + rcount_b;
   if (cudaDeviceSynchronize() != cudaSuccess) return SPECDEC_ERR_CUDA;
   free_workspace(h);
   void* p = nullptr;
@@ -94,6 +96,8 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   h->ws.base = p;
   h->ws.row_stats = reinterpret_cast<float2*>(c);
   c += stats_b;
+  h->ws.row_tau = reinterpret_cast<float*>(c);
+  c += tau_b;
   h->ws.status = reinterpret_cast<uint64_t*>(c);
   c += status_b;
   h->ws.gkeys = reinterpret_cast<uint64_t*>(c);
@@ -226,7 +230,9 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
     }
     kern<<<h->num_sms * ctas, kStreamThreads, smem, st>>>(P);
   } else if (path == SPECDEC_PATH_SWEEP) {
-    if (h->sweep_threads == 512)
+    if (P.topk || P.topp)
+      sweep_row_kernel<TT, 512, 2, true><<<h->num_sms * 2, 512, 0, st>>>(P);
+    else if (h->sweep_threads == 512)
       sweep_row_kernel<TT, 512, 2><<<h->num_sms * 2, 512, 0, st>>>(P);
     else if (h->sweep_threads == 256)
       sweep_row_kernel<TT, 256, 4><<<h->num_sms * 4, 256, 0, st>>>(P);
@@ -316,13 +322,12 @@ int specdec_reserve(specdec_handle_t h, int64_t max_draft_positions, int max_bat
   return alloc_workspace(h, h->res_rows, h->res_b);
 }
 
-int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, int dtype,
-                                const float* draft_probs, const int32_t* draft_ids,
-                                const int32_t* cu_num_draft_tokens, int B, int V, float T,
-                                uint64_t seed, uint64_t request_offset, int32_t* out_tokens,
-                                int32_t* out_num_accepted, float* out_beta,
-                                float* out_target_prob, float* out_draft_prob,
-                                int32_t* out_accept, void* stream) {
+int specdec_rejection_sample_topk_topp(
+    specdec_handle_t h, const void* target_logits, int dtype, const float* draft_probs,
+    const int32_t* draft_ids, const int32_t* cu_num_draft_tokens, int B, int V, float T,
+    const int32_t* top_k, const float* top_p, uint64_t seed, uint64_t request_offset,
+    int32_t* out_tokens, int32_t* out_num_accepted, float* out_beta, float* out_target_prob,
+    float* out_draft_prob, int32_t* out_accept, void* stream) {
   if (!h) return SPECDEC_ERR_INVALID_ARG;
   if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED_DTYPE;
   if (B <= 0 || V <= 0 || V > (1 << 30)) return SPECDEC_ERR_INVALID_ARG;
@@ -358,6 +363,9 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
   P.defer_list = h->ws.defer_list;
   P.rpart = h->ws.rpart;
   P.rcount = h->ws.rcount;
+  P.topk = T > 0.0f ? top_k : nullptr;   // the greedy path keeps the argmax either way
+  P.topp = T > 0.0f ? top_p : nullptr;
+  P.row_tau = (P.topk || P.topp) ? h->ws.row_tau : nullptr;
   P.rslices = (int)std::min<int64_t>(kRaceMaxSlices, std::max<int64_t>(1, (V + 4095) / 4096));
   P.rslice_len = (int)round_up((V + P.rslices - 1) / P.rslices, 8);
   P.defer_count = reinterpret_cast<int32_t*>(h->small + 1);
@@ -381,6 +389,7 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
   P.sched = reinterpret_cast<unsigned long long*>(h->small + 2);
   int path = h->path_override == SPECDEC_PATH_AUTO ? SPECDEC_PATH_SWEEP : h->path_override;
   if (!draft_probs) path = SPECDEC_PATH_SWEEP;  // one-hot drafts: the sweep kernel handles them
+  if (P.topk || P.topp) path = SPECDEC_PATH_SWEEP;  // so do adjusted (top-k / top-p) rows
   if (path == SPECDEC_PATH_STREAM && !P.vec_ok) path = SPECDEC_PATH_SWEEP;
   FusedConfig f;
   if (path == SPECDEC_PATH_FUSED) {
@@ -392,6 +401,19 @@ int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, i
   h->last_cluster = path == SPECDEC_PATH_FUSED ? f.C : (path == SPECDEC_PATH_PAIR ? 2 : 0);
   return dtype == SPECDEC_BF16 ? launch_sampling<__nv_bfloat16>(h, P, f, path, st)
                                : launch_sampling<float>(h, P, f, path, st);
+}
+
+int specdec_rejection_sample_ex(specdec_handle_t h, const void* target_logits, int dtype,
+                                const float* draft_probs, const int32_t* draft_ids,
+                                const int32_t* cu_num_draft_tokens, int B, int V, float T,
+                                uint64_t seed, uint64_t request_offset, int32_t* out_tokens,
+                                int32_t* out_num_accepted, float* out_beta,
+                                float* out_target_prob, float* out_draft_prob,
+                                int32_t* out_accept, void* stream) {
+  return specdec_rejection_sample_topk_topp(h, target_logits, dtype, draft_probs, draft_ids,
+                                            cu_num_draft_tokens, B, V, T, nullptr, nullptr, seed,
+                                            request_offset, out_tokens, out_num_accepted, out_beta,
+                                            out_target_prob, out_draft_prob, out_accept, stream);
 }
 
 int specdec_rejection_sample(specdec_handle_t h, const void* target_logits, int dtype,

@@ -169,3 +169,34 @@ def from_rows(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
     return Workload(name=name, B=len(gam), V=target_logits.shape[-1], dtype=dtype, T=float(T),
                     seed=seed, target_logits=target_logits, draft_probs=draft_probs,
                     draft_ids=draft_ids.to(torch.int32), cu=cu.to(torch.int32))
+
+
+TOP_K_CHOICES = (1, 2, 5, 20, 50, 200, 1000)
+TOP_P_CHOICES = (0.99, 0.95, 0.9, 0.8, 0.5, 0.2)
+
+
+def make_top_k_top_p(B: int, V: int, seed: int, top_k: int | None = None,
+                     top_p: float | None = None, device="cpu"):
+    """Per-request top-k (int32 [B]) and top-p (float32 [B]) settings.
+
+    With ``top_k`` / ``top_p`` given, every request gets that value.  Otherwise
+    a seeded mix: a fifth of the requests use top-k only, a fifth top-p only,
+    two fifths both, the rest neither, with values drawn from common settings
+    plus the edge values the interface defines (k = V - 1, V, V + 7, 0 and -1;
+    p = 0, 1e-6, 1 and 1.5)."""
+    if top_k is not None or top_p is not None:
+        k = torch.full((B,), 0 if top_k is None else int(top_k), dtype=torch.int32)
+        p = torch.full((B,), 1.0 if top_p is None else float(top_p), dtype=torch.float32)
+        return k.to(device), p.to(device)
+    g = torch.Generator()
+    g.manual_seed(seed)
+    ks = list(TOP_K_CHOICES) + [V - 1, V, V + 7, 0, -1]
+    ps = list(TOP_P_CHOICES) + [0.0, 1e-6, 1.0, 1.5]
+    kind = torch.randint(0, 5, (B,), generator=g)
+    ki = torch.randint(0, len(ks), (B,), generator=g)
+    pi = torch.randint(0, len(ps), (B,), generator=g)
+    k = torch.tensor([ks[i] for i in ki.tolist()], dtype=torch.int32)
+    p = torch.tensor([ps[i] for i in pi.tolist()], dtype=torch.float32)
+    k = torch.where((kind == 0) | (kind == 2) | (kind == 3), k, torch.zeros_like(k))
+    p = torch.where((kind == 1) | (kind == 2) | (kind == 3), p, torch.ones_like(p))
+    return k.to(device), p.to(device)

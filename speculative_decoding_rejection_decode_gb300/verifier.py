@@ -12,7 +12,8 @@ from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_FU
                    SPECDEC_PATH_TWO_PASS, specdec_create, specdec_destroy,
                    specdec_get_error, specdec_last_path, specdec_neg_log_uniform,
                    specdec_rejection_sample, specdec_rejection_sample_ex,
-                   specdec_rejection_sample_noalloc, specdec_reserve,
+                   specdec_rejection_sample_noalloc, specdec_rejection_sample_topk_topp,
+                   specdec_reserve,
                    specdec_set_path, specdec_set_timing_events, specdec_status_string,
                    specdec_uniform)
 
@@ -101,9 +102,12 @@ class Verifier:
                  draft_ids: torch.Tensor, cu_num_draft_tokens: torch.Tensor, T: float, seed: int,
                  *, with_beta: bool = True, extended: bool = False,
                  out: VerifyOutput | None = None, n_draft: int | None = None,
-                 request_offset: int = 0) -> VerifyOutput:
+                 request_offset: int = 0, top_k: torch.Tensor | None = None,
+                 top_p: torch.Tensor | None = None) -> VerifyOutput:
         """Runs one verify step on the current torch stream.  ``n_draft`` (= cu[B])
-        avoids a host read of cu when output tensors must be allocated."""
+        avoids a host read of cu when output tensors must be allocated.
+        ``top_k`` (int32 [B]) / ``top_p`` (float32 [B]) restrict the target
+        distribution per request (specdec_rejection_sample_topk_topp)."""
         for t in (target_logits, draft_ids, cu_num_draft_tokens):
             if t.device != self.device or not t.is_contiguous():
                 raise ValueError("inputs must be contiguous tensors on the verifier's device")
@@ -120,6 +124,10 @@ class Verifier:
         if draft_ids.dtype != torch.int32 or cu_num_draft_tokens.dtype != torch.int32:
             raise TypeError("draft_ids and cu_num_draft_tokens must be int32")
         B = cu_num_draft_tokens.numel() - 1
+        for t, dt, name in ((top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p")):
+            if t is not None and (t.device != self.device or t.dtype != dt or t.numel() != B
+                                  or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous {dt} tensor of B entries on the device")
         V = target_logits.shape[-1]
         if out is None:
             nd = int(cu_num_draft_tokens[-1]) if n_draft is None else int(n_draft)
@@ -133,7 +141,13 @@ class Verifier:
                 out.draft_prob = torch.empty(nd, dtype=torch.float32, **kw)
                 out.accept = torch.empty(nd, dtype=torch.int32, **kw)
         stream = _stream_handle(self.device)
-        if (out.target_prob is not None or out.draft_prob is not None or out.accept is not None
+        if top_k is not None or top_p is not None:
+            rc = specdec_rejection_sample_topk_topp(
+                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),
+                _ptr(cu_num_draft_tokens), B, V, float(T), _ptr(top_k), _ptr(top_p), int(seed),
+                int(request_offset), _ptr(out.tokens), _ptr(out.num_accepted), _ptr(out.beta),
+                _ptr(out.target_prob), _ptr(out.draft_prob), _ptr(out.accept), stream)
+        elif (out.target_prob is not None or out.draft_prob is not None or out.accept is not None
                 or request_offset):
             rc = specdec_rejection_sample_ex(
                 self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),

@@ -28,10 +28,29 @@ def run_gpu(verifier, w: Workload, extended: bool = True):
     return res
 
 
-def run_oracle(w: Workload):
+def run_oracle(w: Workload, top_k=None, top_p=None):
     q = None if w.draft_probs is None else w.draft_probs.cpu().numpy()
+    tk = None if top_k is None else np.asarray(top_k.cpu() if hasattr(top_k, "cpu") else top_k)
+    tp = None if top_p is None else np.asarray(top_p.cpu() if hasattr(top_p, "cpu") else top_p)
     return oracle.rejection_sample(to_numpy_logits(w.target_logits), q, w.draft_ids.cpu().numpy(),
-                                   w.cu.cpu().numpy(), w.T, w.seed)
+                                   w.cu.cpu().numpy(), w.T, w.seed, top_k=tk, top_p=tp)
+
+
+def run_gpu_adj(verifier, w: Workload, top_k, top_p, extended: bool = True):
+    """The top-k / top-p entry point (top_k / top_p: torch tensors or None)."""
+    dev = verifier.device
+    wd = w.to(dev)
+    tk = None if top_k is None else top_k.to(dev)
+    tp = None if top_p is None else top_p.to(dev)
+    out = verifier(wd.target_logits, wd.draft_probs, wd.draft_ids, wd.cu, w.T, w.seed,
+                   extended=extended, n_draft=w.n_draft, top_k=tk, top_p=tp)
+    torch.cuda.synchronize(dev)
+    res = dict(tokens=out.tokens.cpu().numpy(), num_accepted=out.num_accepted.cpu().numpy(),
+               beta=out.beta.cpu().numpy())
+    if extended:
+        res.update(p_x=out.target_prob.cpu().numpy(), q_x=out.draft_prob.cpu().numpy(),
+                   accept=out.accept.cpu().numpy())
+    return res
 
 
 def compare(w: Workload, g: dict, r: oracle.OracleResult, exact: bool = False,
@@ -77,7 +96,7 @@ def flag_budget_ok(flagged: int, n_requests: int) -> bool:
     return flagged <= max(1, math.ceil(1e-4 * n_requests))
 
 
-def sampled_oracle(w: Workload, requests):
+def sampled_oracle(w: Workload, requests, top_k=None, top_p=None):
     """Oracle results for a few requests of a large workload, one at a time,
     scattered into full-size arrays (entries of other requests are unset)."""
     cu = w.cu.cpu().numpy().astype(np.int64)
@@ -86,12 +105,16 @@ def sampled_oracle(w: Workload, requests):
                               beta=np.zeros(n_d), p_x=np.zeros(n_d), q_x=np.zeros(n_d),
                               accept=np.zeros(n_d, np.int32), pos_near_tie=np.zeros(n_d, np.int32),
                               near_tie=np.zeros(B, np.int32), status=0)
+    tk = None if top_k is None else top_k.cpu().numpy()
+    tp = None if top_p is None else top_p.cpu().numpy()
     for b in requests:
         d0, d1 = cu[b], cu[b + 1]
         t0, t1 = d0 + b, d1 + b + 1
         tgt = to_numpy_logits(w.target_logits[t0:t1])
         q = None if w.draft_probs is None else w.draft_probs[d0:d1].cpu().numpy()
-        one = oracle.verify_request(int(b), tgt, q, w.draft_ids[d0:d1].cpu().numpy(), w.T, w.seed)
+        one = oracle.verify_request(int(b), tgt, q, w.draft_ids[d0:d1].cpu().numpy(), w.T, w.seed,
+                                    top_k=0 if tk is None else int(tk[b]),
+                                    top_p=1.0 if tp is None else float(tp[b]))
         res.tokens[t0:t1] = one.tokens
         res.num_accepted[b] = one.num_accepted[0]
         res.beta[d0:d1] = one.beta

@@ -1,0 +1,174 @@
+"""Top-k / top-p adjusted targets (the vllbc page's Section 2.2 note: top-k and
+top-p fold into the adjusted p before the same rejection test): the CUDA
+library through specdec_rejection_sample_topk_topp against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import stat_checks as sc
+from gpu_helpers import (compare, flag_budget_ok, run_gpu, run_gpu_adj, run_oracle,
+                         sampled_oracle)
+from speculative_decoding_rejection_decode_gb300.inputs import (from_rows, make_config,
+                                                                make_top_k_top_p, make_workload)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def V():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_rejection_decode_gb300 import Verifier
+    v = Verifier(0)
+    yield v
+    v.close()
+
+
+def _check(V, w, tk, tp, budget=True):
+    g = run_gpu_adj(V, w, tk, tp)
+    assert V.get_error() == 0
+    r = run_oracle(w, tk, tp)
+    st = compare(w, g, r)
+    if budget:
+        assert flag_budget_ok(st["flagged"], st["requests"]), st
+    return g, r
+
+
+@pytest.mark.parametrize("idx", [0, 1, 3])
+def test_standard_workloads_with_mixed_settings(V, idx):
+    w = make_config(idx, device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=100 + idx)
+    _check(V, w, tk, tp)
+
+
+@pytest.mark.parametrize("top_k,top_p", [(50, 1.0), (0, 0.9), (20, 0.8), (1, 1.0), (0, 0.0)])
+def test_large_vocab_bf16_uniform_settings(V, top_k, top_p):
+    w = make_config(4, device="cuda", B=12)
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=0, top_k=top_k, top_p=top_p)
+    _check(V, w, tk, tp)
+
+
+def test_full_size_large_workload_sampled(V):
+    w = make_config(4, device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=44)
+    g = run_gpu_adj(V, w, tk, tp)
+    assert V.get_error() == 0
+    cu = w.cu.cpu().numpy()
+    sc.check_e_layout(g["tokens"], g["num_accepted"], w.draft_ids.cpu().numpy(), cu, w.V)
+    rng = np.random.default_rng(44)
+    reqs = sorted(set([0, 1, w.B - 1] + list(rng.choice(w.B, 9, replace=False))))
+    r = sampled_oracle(w, reqs, tk, tp)
+    st = compare(w, g, r, requests=reqs)
+    assert st["flagged"] <= 1
+
+
+@pytest.mark.parametrize("Vsz,dtype", [(8, "f32"), (8, "bf16"), (100, "f32"), (4097, "bf16"),
+                                       (4099, "f32"), (12345, "f32"), (65536, "bf16"),
+                                       (151936, "f32")])
+def test_vocab_sizes_and_tails(V, Vsz, dtype):
+    w = make_workload(name="adj tails", B=24, gamma=(0, 6), V=Vsz, dtype=dtype, T=0.9, seed=71,
+                      target_std=2.0, noise_std=0.8, device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=Vsz)
+    _check(V, w, tk, tp)
+
+
+@pytest.mark.parametrize("T", [0.05, 0.5, 2.5, 10.0])
+def test_temperatures(V, T):
+    w = make_workload(name="adj temps", B=24, gamma=5, V=30000, dtype="bf16", T=T, seed=73,
+                      target_std=3.0, noise_std=1.0, draft_T=T, device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=int(T * 100))
+    _check(V, w, tk, tp)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ties_signed_zero_and_masked_entries(V, dtype):
+    # integer logits: large tie groups at every cut; -0.0 / +0.0 are one value;
+    # -inf entries are never kept and never counted as mass
+    g0 = torch.Generator().manual_seed(5)
+    B, gam, Vs = 32, 3, 3000
+    tgt = torch.randint(-4, 5, (B * (gam + 1), Vs), generator=g0).float()
+    neg0 = torch.rand(tgt.shape, generator=g0) < 0.5
+    tgt = torch.where((tgt == 0) & neg0, torch.tensor(-0.0), tgt)
+    tgt[:, 1000:1500] = -float("inf")
+    tgt[::5, 10:] = -float("inf")          # rows with only 10 finite logits (k beyond them)
+    if dtype == "bf16":
+        tgt = tgt.bfloat16()
+    q = torch.softmax(torch.randn(B * gam, Vs, generator=g0), -1)
+    ids = torch.multinomial(q, 1, generator=g0).view(-1).int()
+    w = from_rows(tgt, q, ids, [gam] * B, T=1.0, seed=12).to("cuda")
+    for tk, tp in [make_top_k_top_p(B, Vs, seed=3), make_top_k_top_p(B, Vs, 0, top_k=200),
+                   make_top_k_top_p(B, Vs, 0, top_k=20), make_top_k_top_p(B, Vs, 0, top_p=0.5)]:
+        _check(V, w, tk, tp)
+
+
+def test_onehot_drafts_with_settings(V):
+    w = make_workload(name="adj onehot", B=48, gamma=(0, 7), V=50000, dtype="bf16", T=1.0,
+                      seed=77, ids="argmax0.75", device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=7)
+    g, _ = _check(V, w, tk, tp)
+    assert np.abs(g["beta"] - g["p_x"]).max() <= 1e-6
+
+
+def test_switched_off_matches_the_plain_call(V):
+    w = make_config(3, device="cuda", B=40, V=20000)
+    plain = run_gpu(V, w)
+    off_k = torch.full((w.B,), 0, dtype=torch.int32)
+    off_p = torch.full((w.B,), 1.0)
+    for tk, tp in [(None, None), (off_k, None), (None, off_p), (off_k, off_p)]:
+        g = run_gpu_adj(V, w, tk, tp)
+        for key in plain:
+            assert np.array_equal(g[key], plain[key]), key
+
+
+def test_top_k_one_reproduces_greedy_tokens(V):
+    w = make_workload(name="adj k1", B=64, gamma=(1, 6), V=20000, dtype="f32", T=1.0, seed=79,
+                      ids="argmax0.75", device="cuda")
+    q = torch.softmax(torch.randn(w.n_draft, w.V, generator=torch.Generator().manual_seed(1)), -1)
+    ws = from_rows(w.target_logits.cpu(), q, w.draft_ids.cpu(), np.diff(w.cu.cpu().numpy()).tolist(),
+                   T=1.0, seed=79).to("cuda")
+    greedy = from_rows(w.target_logits.cpu(), None, w.draft_ids.cpu(),
+                       np.diff(w.cu.cpu().numpy()).tolist(), T=0.0, seed=0).to("cuda")
+    gg = run_gpu(V, greedy, extended=False)
+    tk, tp = make_top_k_top_p(w.B, w.V, 0, top_k=1)
+    g = run_gpu_adj(V, ws, tk, tp)
+    assert np.array_equal(g["tokens"], gg["tokens"])
+    assert np.array_equal(g["num_accepted"], gg["num_accepted"])
+
+
+def test_deterministic_across_calls(V):
+    w = make_config(3, device="cuda", B=40, V=20000)
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=9)
+    a = run_gpu_adj(V, w, tk, tp)
+    b = run_gpu_adj(V, w, tk, tp)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("top_k,top_p", [(3, 1.0), (0, 0.7), (5, 0.8)])
+def test_output_distribution_follows_the_adjusted_target(V, top_k, top_p):
+    dev = V.device
+
+    def run(tgt, q, ids, cu, T, seed, k, p):
+        B = len(cu) - 1
+        out = V(torch.from_numpy(tgt).to(dev), torch.from_numpy(q).to(dev),
+                torch.from_numpy(ids).to(dev), torch.from_numpy(cu).to(dev), T, seed,
+                extended=True, n_draft=int(cu[-1]),
+                top_k=torch.full((B,), k, dtype=torch.int32, device=dev),
+                top_p=torch.full((B,), p, dtype=torch.float32, device=dev))
+        torch.cuda.synchronize(dev)
+        return (out.tokens.cpu().numpy(), out.num_accepted.cpu().numpy(),
+                out.accept.cpu().numpy(), out.beta.cpu().numpy().astype(np.float64))
+    out = sc.check_adjusted_distribution(run, top_k, top_p, n=400_000)
+    assert out["slot0"] > sc.P_MIN
+    assert out["residual"] > sc.P_MIN
+    assert out["bonus"] > sc.P_MIN
+    assert out["accept_z"] < 3.0
+    assert out["beta_err"] < 1e-6
+
+
+def test_argument_checks(V):
+    w = make_config(1, device="cuda")
+    with pytest.raises(ValueError):
+        run_gpu_adj(V, w, torch.zeros(w.B + 1, dtype=torch.int32), None)
+    with pytest.raises(ValueError):
+        run_gpu_adj(V, w, None, torch.ones(w.B, dtype=torch.float64))
