@@ -389,6 +389,17 @@ def main():
         "wall_s_timed_region": t_wall,
     }
 
+    if tk is not None:
+        # one more step with the selection counters on (outside the timed region)
+        ctr = torch.zeros(8, dtype=torch.int64, device=dev)
+        v.set_adjust_counters(ctr)
+        step()
+        torch.cuda.synchronize(dev)
+        v.set_adjust_counters(None)
+        c = ctr.cpu().tolist()
+        result["adjust_selection_per_step"] = {
+            "adjusted_rows": c[0], "sample_edge_in_tail": c[1], "edge_past_cut": c[2],
+            "key_refinement_passes": c[3], "rows_without_threshold": c[4]}
     nacc = out.num_accepted.double()
     result["acceptance"] = {
         # accepted drafts / proposed drafts (the timinsight guide's definition)

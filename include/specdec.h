@@ -200,6 +200,15 @@ int specdec_set_path(specdec_handle_t h, int path);
  * Pass NULL, NULL to stop.  The events stay owned by the caller. */
 int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after_rows);
 
+/* Profiling hook for adjusted (top-k / top-p) rows: when set, every later call
+ * adds to device_counters (device memory, 8 uint64 entries, owned by the
+ * caller, zeroed by the caller): [0] adjusted rows, [1] rows whose sampled
+ * estimate put the edge in the tail, [2] rows whose edge lay past the
+ * estimated cut (both take a selection over the whole row), [3] key-refinement
+ * passes, [4] rows left without a threshold (NaN logits), [5..7] unused.
+ * NULL stops. */
+int specdec_set_adjust_counters(specdec_handle_t h, uint64_t* device_counters);
+
 /* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
  * _STREAM, _PAIR or _GREEDY), and the cluster size of a cluster path (0 otherwise). */
 int specdec_last_path(specdec_handle_t h, int* path, int* cluster_size);

@@ -70,6 +70,7 @@ _get_error = _fn("specdec_get_error", _i32, _vp, ctypes.POINTER(_i32), _vp)
 _set_path = _fn("specdec_set_path", _i32, _vp, _i32)
 _set_events = _fn("specdec_set_timing_events", _i32, _vp, _vp, _vp)
 _last_path = _fn("specdec_last_path", _i32, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
+_set_adj_ctr = _fn("specdec_set_adjust_counters", _i32, _vp, _vp)
 _uniform = _fn("specdec_uniform", _i32, _u64, _u64, _u64, _u32, _u64, _i64, _vp, _vp)
 _neg_log = _fn("specdec_neg_log_uniform", _i32, _u32, _i64, _vp, _vp)
 _rs_noalloc = _fn("specdec_rejection_sample_noalloc", _i32, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
@@ -116,6 +117,10 @@ def specdec_set_timing_events(h: int, before_rows, after_rows) -> int:
     return _set_events(h, before_rows, after_rows)
 
 
+def specdec_set_adjust_counters(h: int, device_counters) -> int:
+    return _set_adj_ctr(h, device_counters)
+
+
 def specdec_get_error(h: int, stream) -> tuple[int, int]:
     e = _i32(0)
     rc = _get_error(h, ctypes.byref(e), stream)
@@ -160,6 +165,6 @@ def specdec_destroy(h: int) -> int:
 EXPORTED = ["specdec_create", "specdec_reserve", "specdec_rejection_sample",
             "specdec_rejection_sample_ex", "specdec_rejection_sample_topk_topp",
             "specdec_get_error", "specdec_set_path",
-            "specdec_set_timing_events",
+            "specdec_set_timing_events", "specdec_set_adjust_counters",
             "specdec_last_path", "specdec_uniform", "specdec_neg_log_uniform",
             "specdec_rejection_sample_noalloc", "specdec_status_string", "specdec_destroy"]

@@ -25,8 +25,6 @@
 // Non-template kernels are `static`: each translation unit that launches them
 // (the handle path and the allocation-free path) keeps its own copy.
 
-#include <type_traits>
-
 #include "device_common.cuh"
 
 namespace specdec {
@@ -66,6 +64,7 @@ struct Params {
   const int32_t* topk;     // [B] per-request top-k or null (adjusted rows, sweep kernel only)
   const float* topp;       // [B] per-request top-p or null
   float* row_tau;          // [cap_rows] logit threshold of each adjusted row, or null
+  unsigned long long* adj_ctr;  // [kAdjCounters] selection statistics (profiling), or null
   uint32_t* err;           // [1] sticky device error word
   int64_t cap_rows;
   int cap_b;
@@ -613,32 +612,48 @@ __device__ __forceinline__ void sweep1(const TT* row, int lo, int hi, bool vec, 
 // Top-k / top-p adjusted target rows (the vllbc page's Section 2.2 note: top-k
 // and top-p fold into the adjusted p before the same rejection test).
 //
-// Kept set of a row with e(v) = exp2((l_v - M) c):
+// Kept set of a row, with masses e(v) of the logits:
 //   top-k (1 <= k < V): v with fewer than k logits above l_v (ties at the k-th
 //                       largest logit all stay);
 //   top-p (P < 1):      v with A(v) = 0 or A(v) < P * S_k, A(v) the mass of the
 //                       logits above l_v and S_k the mass kept by top-k.
 // Both are a threshold on the logit: the kept set is {v : l_v >= tau}.  tau is
-// found by a selection over the row while it is still in L2: a first pass
-// bins every entry by z = (M - l) c (64 bins per unit of z, so the bins are
-// linear in the logit near the top of the row, where the edge usually falls;
-// z >= 32 shares the last bin), then each further pass splits the chosen bin
-// into 1024 sub-bins, by finer z first and by the order-preserving 32-bit key
-// of the logit after that, until the chosen sub-bin holds a single logit
-// value.  Counts are exact; masses are integers (pow2_neg(z) scaled by 2^F
-// with V 2^F <= 2^62), so the shared-memory histograms add up the same way in
-// any order, the result does not depend on thread timing, and the top-p test
+// found by a selection over the row while it is still in L2:
+//   1. an estimate: a histogram of one 16-byte vector in 16, binned by
+//      z = (M - l) c (64 bins per unit of z), gives the z by which the edge
+//      should have been passed; the cut Zc is set a margin beyond it;
+//   2. the entries with z < Zc go into 2048 bins of width 2^-a (a as fine as
+//      the cut allows) with their count, mass and smallest / largest logit
+//      key; every other entry is only counted (and its mass summed, when the
+//      top-p bound needs the whole row) in registers;
+//   3. the bin where the criterion is met either holds one logit value (done)
+//      or is split by its keys into 1024 sub-bins, again until one value is
+//      left.
+// When the edge lies beyond Zc (or in a row holding -inf or NaN at the edge)
+// step 2 runs again with 64 bins per unit and a last bin that takes the rest.
+// Counts are exact; masses are integers (pow2_neg(z) scaled by 2^F with
+// V 2^F <= 2^62), so the shared-memory histograms add up the same way in any
+// order, the result does not depend on thread timing, and the top-p test
 // (double)A < (double)P * (double)S_k sees the numbers a CPU restatement sees.
 // ---------------------------------------------------------------------------
 constexpr int kAdjBins1 = 2048;
 constexpr int kAdjBins2 = 1024;
-constexpr float kAdjZ1 = 64.0f;          // level-1 bins per unit of z
-constexpr float kAdjZ2 = 65536.0f;       // level-2 sub-bins per unit of z (kAdjZ1 * kAdjBins2)
-constexpr int kAdjMaxKeyLevels = 4;      // 1024^4 > 2^32: key levels always end on one value
+constexpr int kAdjSample = 16;       // the estimate reads one vector (or element) in 16
+constexpr int kAdjMaxKeyLevels = 4;  // 1024^4 > 2^32: key levels always end on one value
+
+// Selection statistics (specdec_set_adjust_counters): adjusted rows, rows whose
+// sample put the edge in the last bin, rows whose edge lay past the cut,
+// key-refinement passes, rows left without a threshold.
+enum AdjCounter { kAdjRows = 0, kAdjTail, kAdjMiss, kAdjKeyPass, kAdjNone, kAdjCounters = 8 };
+__device__ __forceinline__ void adj_count(unsigned long long* ctr, int i) {
+  if (ctr && threadIdx.x == 0) atomicAdd(ctr + i, 1ull);
+}
 
 struct AdjShared {
   uint32_t cnt1[kAdjBins1];
   unsigned long long mass1[kAdjBins1];
+  uint32_t kmin1[kAdjBins1];
+  uint32_t kmax1[kAdjBins1];
   uint32_t cnt2[kAdjBins2];
   unsigned long long mass2[kAdjBins2];
   uint32_t kmin2[kAdjBins2];
@@ -681,68 +696,56 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// One histogram pass over the row.
-//   mode 1: every entry into the level-1 bins (count, and mass when need_mass);
-//   mode 2: entries of level-1 bin j1 (< last) into sub-bins of z / 65536;
-//   mode 3: entries with key in [lo, hi] (and, when j1 >= 0, in level-1 bin j1)
-//           into sub-bins of `w` consecutive keys, counted down from hi.
-// At every level bin 0 holds the largest logits.
-// Modes 2 and 3 also keep each sub-bin's smallest and largest key.
-template <typename TT, int NT>
-__device__ __forceinline__ void adj_pass(const TT* row, int V, bool vec, float M, float c,
-                                         float fscale, int mode, bool need_mass, int j1,
-                                         uint32_t lo, uint32_t hi, uint32_t w, uint64_t pol,
-                                         AdjShared& A) {
+// Level-1 geometry: bins of width 1/scale in z (scale a power of two).  With
+// catch_all the last bin also takes every z past the grid, NaN included;
+// otherwise only z < cut is binned and the rest is "far".
+struct AdjGrid {
+  float scale;
+  float cut;
+  bool catch_all;
+};
+
+__device__ __forceinline__ int adj_bin1(float z, const AdjGrid& g) {
+  if (g.catch_all) {
+    const float y = z * g.scale;
+    return y < (float)(kAdjBins1 - 1) ? (int)y : kAdjBins1 - 1;
+  }
+  if (!(z < g.cut)) return -1;
+  const int b = (int)(z * g.scale);
+  return b < kAdjBins1 ? b : kAdjBins1 - 1;  // the cut lies inside the grid; guard only
+}
+
+// Visits every entry of the row (or, with kSampled, one 16-byte vector in 16,
+// one element in 16 on unaligned rows) through f(x).
+template <typename TT, int NT, bool kSampled, typename Fn>
+__device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64_t pol, Fn&& f) {
   constexpr int kEl = 16 / sizeof(TT);
-  auto add = [&](float x) {
-    const float z = (M - x) * c;
-    const float y = z * kAdjZ1;
-    const int b1 = y < (float)(kAdjBins1 - 1) ? (int)y : kAdjBins1 - 1;
-    if (mode == 1) {
-      atomicAdd(&A.cnt1[b1], 1u);
-      if (need_mass) atomicAdd(&A.mass1[b1], __float2ull_rn(pow2_neg(z) * fscale));
-      return;
-    }
-    int s;
-    uint32_t k = order_key(x);
-    if (mode == 2) {
-      if (b1 != j1) return;
-      s = (int)(z * kAdjZ2) - j1 * kAdjBins2;
-    } else {
-      if (k < lo || k > hi || (j1 >= 0 && b1 != j1)) return;
-      s = (int)((hi - k) / w);  // sub-bin 0 holds the largest keys, like every other level
-    }
-    if ((unsigned)s >= (unsigned)kAdjBins2) return;  // cannot happen for the bins chosen above
-    atomicAdd(&A.cnt2[s], 1u);
-    atomicAdd(&A.mass2[s], __float2ull_rn(pow2_neg(z) * fscale));
-    atomicMin(&A.kmin2[s], k);
-    atomicMax(&A.kmax2[s], k);
-  };
+  constexpr int kStep = kSampled ? kAdjSample : 1;
   const int tid = threadIdx.x;
   if (vec) {
     const uint4* rv = reinterpret_cast<const uint4*>(row);
     const int nv = V / kEl;
-    int j = tid;
-    for (; j + 3 * NT < nv; j += 4 * NT) {
-      uint4 a[4];
+    int j = tid * kStep;
+    for (; j + NT * kStep < nv; j += 2 * NT * kStep) {
+      uint4 a[2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = ldg_hint(rv + j + u * NT, pol);
+      for (int u = 0; u < 2; ++u) a[u] = ldg_hint(rv + j + u * NT * kStep, pol);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         float x[kEl];
         unpack16<TT>(a[u], x);
 #pragma unroll
-        for (int e = 0; e < kEl; ++e) add(x[e]);
+        for (int e = 0; e < kEl; ++e) f(x[e]);
       }
     }
-    for (; j < nv; j += NT) {
+    for (; j < nv; j += NT * kStep) {
       float x[kEl];
       unpack16<TT>(ldg_hint(rv + j, pol), x);
 #pragma unroll
-      for (int e = 0; e < kEl; ++e) add(x[e]);
+      for (int e = 0; e < kEl; ++e) f(x[e]);
     }
   } else {
-    for (int v = tid; v < V; v += NT) add(load_logit(row + v));
+    for (int v = tid * kStep; v < V; v += NT * kStep) f(load_logit(row + v));
   }
 }
 
@@ -814,26 +817,42 @@ __device__ __forceinline__ void adj_select(const uint32_t* cnt, const unsigned l
   __syncthreads();
 }
 
-// Refines the level-1 histogram down to the single logit value at which the
-// criterion (see adj_select) is met.  Returns its key and the mass of every
-// entry whose key is >= it; false when no bin qualifies (rows holding NaN).
-template <typename TT, int NT>
-__device__ bool adj_resolve(const TT* row, int V, bool vec, float M, float c, float fscale,
-                            bool by_mass, uint32_t need, double bound, uint64_t pol, AdjShared& A,
-                            uint32_t& key, unsigned long long& kept) {
-  const int tid = threadIdx.x;
-  adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, need, bound, 0ull, A);
-  const int j1 = A.sel;
-  uint32_t above_c = A.ex_cnt;
-  unsigned long long above_m = A.ex_mass;
+// Sum of one value over the block (deterministic).  Ends on a barrier.
+template <int NT>
+__device__ __forceinline__ unsigned long long adj_block_sum(unsigned long long x, AdjShared& A) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  if (lane == 0) A.wmass[warp] = x;
   __syncthreads();
-  if (j1 >= kAdjBins1) return false;
-  // level 2: finer z inside a regular bin; keys below the max for the last bin
-  int mode = j1 < kAdjBins1 - 1 ? 2 : 3;
-  int zf = j1;
-  uint32_t lo = 0, hi = order_key(M);
-  uint32_t w = (uint32_t)(((unsigned long long)hi - lo + kAdjBins2) / kAdjBins2);
+  unsigned long long t = 0;
+  for (int w = 0; w < NT / 32; ++w) t += A.wmass[w];
+  __syncthreads();
+  return t;
+}
+
+// Splits the chosen bin, whose entries are exactly those with keys in
+// [lo, hi] (z is monotone in the logit), by keys into 1024 sub-bins (sub-bin 0
+// holds the largest keys) until the criterion (see adj_select) is met on a
+// single logit value.  above_c / above_m: count and mass of every entry with a
+// key above hi; m_sel: the chosen bin's mass.  Returns the value's key and the
+// mass of every entry whose key is >= it; false when no sub-bin qualifies.
+template <typename TT, int NT>
+__device__ bool adj_refine(const TT* row, int V, bool vec, float M, float c, float fscale,
+                           bool by_mass, uint32_t need, double bound, uint32_t above_c,
+                           unsigned long long above_m, uint32_t lo, uint32_t hi,
+                           unsigned long long m_sel, uint64_t pol, AdjShared& A, uint32_t& key,
+                           unsigned long long& kept, unsigned long long* ctr) {
+  const int tid = threadIdx.x;
+  if (lo > hi) return false;
   for (int level = 0; level <= kAdjMaxKeyLevels; ++level) {
+    if (lo == hi) {
+      key = lo;
+      kept = above_m + m_sel;
+      return true;
+    }
+    const uint32_t w = (uint32_t)(((unsigned long long)hi - lo + kAdjBins2) / kAdjBins2);
+    adj_count(ctr, kAdjKeyPass);
     for (int j = tid; j < kAdjBins2; j += NT) {
       A.cnt2[j] = 0u;
       A.mass2[j] = 0ull;
@@ -841,69 +860,181 @@ __device__ bool adj_resolve(const TT* row, int V, bool vec, float M, float c, fl
       A.kmax2[j] = 0u;
     }
     __syncthreads();
-    adj_pass<TT, NT>(row, V, vec, M, c, fscale, mode, true, zf, lo, hi, w, pol, A);
+    adj_visit<TT, NT, false>(row, V, vec, pol, [&](float x) {
+      const uint32_t k = order_key(x);
+      if (k < lo || k > hi) return;
+      const uint32_t s = (hi - k) / w;
+      if (s >= (uint32_t)kAdjBins2) return;  // cannot happen; guard only
+      atomicAdd(&A.cnt2[s], 1u);
+      atomicAdd(&A.mass2[s], __float2ull_rn(pow2_neg((M - x) * c) * fscale));
+      atomicMin(&A.kmin2[s], k);
+      atomicMax(&A.kmax2[s], k);
+    });
     __syncthreads();
     adj_select<NT>(A.cnt2, A.mass2, kAdjBins2, by_mass, need - above_c, bound, above_m, A);
     const int s = A.sel;
-    bool done = false;
     if (s < kAdjBins2) {
       above_c += A.ex_cnt;
       above_m += A.ex_mass;
       lo = A.kmin2[s];
       hi = A.kmax2[s];
-      done = lo == hi;
-      if (done) {
-        key = lo;
-        kept = above_m + A.mass2[s];
-      }
+      m_sel = A.mass2[s];
     }
     __syncthreads();
     if (s >= kAdjBins2 || lo > hi) return false;
-    if (done) return true;
-    mode = 3;
-    zf = -1;
-    w = (uint32_t)(((unsigned long long)hi - lo + kAdjBins2) / kAdjBins2);
   }
   return false;
 }
 
-// Threshold tau (keep l >= tau) and kept mass S of an adjusted row whose max is
-// M.  Block-wide (every thread of the block calls it with the same arguments).
-// Returns false, leaving tau and S alone, when no threshold exists (NaN rows).
+// Every entry with z < cut (all of them with catch_all) goes into the level-1
+// bins with its count, mass and key range (the others are only counted, and
+// their mass summed when the top-p bound needs the whole row); then the top-k
+// and top-p edges.  Returns false when an edge lies past the grid (only
+// possible without catch_all) or the row holds NaN.
 template <typename TT, int NT>
-__device__ bool adjust_row(const TT* row, int V, bool vec, float M, float c, int top_k,
+__device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float fscale, int top_k,
+                        float top_p, bool use_k, bool use_p, const AdjGrid& g, uint64_t pol,
+                        AdjShared& A, uint32_t& key, unsigned long long& kept,
+                        unsigned long long* ctr) {
+  const int tid = threadIdx.x;
+  for (int j = tid; j < kAdjBins1; j += NT) {
+    A.cnt1[j] = 0u;
+    A.mass1[j] = 0ull;
+    A.kmin1[j] = 0xFFFFFFFFu;
+    A.kmax1[j] = 0u;
+  }
+  __syncthreads();
+  // the far entries' mass matters only for a top-p bound over the whole row
+  const bool far_mass = use_p && !use_k;
+  unsigned long long fm = 0;
+  adj_visit<TT, NT, false>(row, V, vec, pol, [&](float x) {
+    const float z = (M - x) * c;
+    const int b = adj_bin1(z, g);
+    if (b < 0) {
+      if (far_mass) fm += __float2ull_rn(pow2_neg(z) * fscale);
+      return;
+    }
+    const uint32_t k = order_key(x);
+    atomicAdd(&A.cnt1[b], 1u);
+    atomicAdd(&A.mass1[b], __float2ull_rn(pow2_neg(z) * fscale));
+    atomicMin(&A.kmin1[b], k);
+    atomicMax(&A.kmax1[b], k);
+  });
+  __syncthreads();
+  unsigned long long tm = fm;
+  for (int j = tid; j < kAdjBins1; j += NT) tm += A.mass1[j];
+  kept = adj_block_sum<NT>(tm, A);
+  key = 0u;  // below every logit
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool by_mass = pass == 1;
+    if (by_mass ? !use_p : !use_k) continue;
+    const double bound =
+        by_mass ? (top_p > 0.0f ? (double)top_p : 0.0) * (double)kept : 0.0;
+    adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, (uint32_t)top_k, bound, 0ull, A);
+    const int j1 = A.sel;
+    uint32_t ac = 0, lo = 1, hi = 0;
+    unsigned long long am = 0, ms = 0;
+    if (j1 < kAdjBins1) {
+      ac = A.ex_cnt;
+      am = A.ex_mass;
+      lo = A.kmin1[j1];
+      hi = A.kmax1[j1];
+      ms = A.mass1[j1];
+    }
+    __syncthreads();
+    if (!adj_refine<TT, NT>(row, V, vec, M, c, fscale, by_mass, (uint32_t)top_k, bound, ac, am,
+                            lo, hi, ms, pol, A, key, kept, ctr))
+      return false;
+  }
+  return true;
+}
+
+// The cut for the level-1 histogram from a sample of the row: the z (64 bins
+// per unit) by which the sample passes 1.5 times its share of the top-k count,
+// or, for top-p alone, where the sample's tail beyond z (16 times its mass)
+// falls to (1 - P) S, S the row's softmax sum (the tail is made of many light
+// entries, so its estimate is steadier than one of the few heavy ones at the
+// top); plus a margin.  With both, the top-p edge lies inside the top-k set.
+// False when the sample puts the edge in the last bin.
+template <typename TT, int NT>
+__device__ bool adj_estimate(const TT* row, int V, bool vec, float M, float c, float S,
+                             int top_k, float top_p, bool use_k, bool use_p, uint64_t pol,
+                             AdjShared& A, AdjGrid& g) {
+  const int tid = threadIdx.x;
+  const AdjGrid coarse{64.0f, 0.0f, true};
+  for (int j = tid; j < kAdjBins1; j += NT) A.cnt1[j] = 0u;
+  __syncthreads();
+  adj_visit<TT, NT, true>(row, V, vec, pol, [&](float x) {
+    atomicAdd(&A.cnt1[adj_bin1((M - x) * c, coarse)], 1u);
+  });
+  __syncthreads();
+  // mass of a bin taken at its centre, in units of 2^-32
+  unsigned long long tm = 0;
+  for (int j = tid; j < kAdjBins1; j += NT) {
+    A.mass1[j] = (unsigned long long)A.cnt1[j] *
+                 (unsigned long long)exp2f(32.0f - ((float)j + 0.5f) * (1.0f / 64.0f));
+    tm += A.mass1[j];
+  }
+  __syncthreads();
+  const unsigned long long s_sample = adj_block_sum<NT>(tm, A);
+  if (use_k) {
+    // aim past the sample's share of k (a sample that happens to hold more
+    // than its share of the top-k set stays inside)
+    const int share = (top_k + kAdjSample - 1) / kAdjSample;
+    adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, false, (uint32_t)(share + share / 2 + 2), 0.0,
+                   0ull, A);
+  } else {
+    const double p = top_p > 0.0f ? (double)top_p : 0.0;
+    const double tail = (1.0 - p) * (double)S * 4294967296.0 / (double)kAdjSample;
+    adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, true, 0u, (double)s_sample - tail, 0ull, A);
+  }
+  const int j = A.sel;
+  __syncthreads();
+  if (j >= kAdjBins1 - 1) return false;
+  const float z_est = (float)(j + 1) * (1.0f / 64.0f);
+  g.cut = 1.0625f * z_est + 0.5f;
+  // finest power-of-two bin width whose 2048 bins still cover the cut
+  int a = 6;
+  while (a < 24 && (float)kAdjBins1 / (float)(1 << (a + 1)) >= g.cut) ++a;
+  while (a > -8 && (float)kAdjBins1 * exp2f((float)-a) < g.cut) --a;
+  g.scale = exp2f((float)a);
+  g.catch_all = false;
+  return true;
+}
+
+// Threshold tau (keep l >= tau) and kept mass S of an adjusted row whose max is
+// M; S holds the row's softmax sum on entry.  Block-wide (every thread of the
+// block calls it with the same arguments).  Returns false, leaving tau and S
+// alone, when no threshold exists (NaN rows).
+template <typename TT, int NT>
+__device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M, float c, int top_k,
                            float top_p, bool use_k, bool use_p, uint64_t pol, AdjShared& A,
-                           float& tau, float& S) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // masses are e * 2^F with V * 2^F <= 2^62
+                           float& tau, float& S, unsigned long long* ctr) {
+  // masses are pow2_neg(z) * 2^F with V * 2^F <= 2^62
   const int lg = V > 1 ? 32 - __clz(V - 1) : 0;
   const int F = 62 - lg;
   const float fscale = __int_as_float((127 + F) << 23);
   const double unscale = __longlong_as_double((long long)(1023 - F) << 52);
-  for (int j = tid; j < kAdjBins1; j += NT) {
-    A.cnt1[j] = 0u;
-    A.mass1[j] = 0ull;
+  uint32_t key = 0u;
+  unsigned long long kept = 0ull;
+  AdjGrid g{64.0f, 0.0f, true};
+  bool ok = false;
+  adj_count(ctr, kAdjRows);
+  if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g)) {
+    ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, g, pol, A, key,
+                         kept, ctr);
+    if (!ok) adj_count(ctr, kAdjMiss);
+  } else {
+    adj_count(ctr, kAdjTail);
   }
-  __syncthreads();
-  adj_pass<TT, NT>(row, V, vec, M, c, fscale, 1, true, 0, 0u, 0u, 1u, pol, A);
-  __syncthreads();
-  unsigned long long tm = 0;
-  for (int j = tid; j < kAdjBins1; j += NT) tm += A.mass1[j];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tm += __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-  if (lane == 0) A.wmass[warp] = tm;
-  __syncthreads();
-  unsigned long long kept = 0;
-  for (int w = 0; w < NT / 32; ++w) kept += A.wmass[w];
-  __syncthreads();
-  uint32_t key = 0u;  // below every logit
-  if (use_k && !adj_resolve<TT, NT>(row, V, vec, M, c, fscale, false, (uint32_t)top_k, 0.0, pol,
-                                    A, key, kept))
+  if (!ok) {
+    const AdjGrid full{64.0f, 0.0f, true};
+    ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, full, pol, A, key,
+                         kept, ctr);
+  }
+  if (!ok) {
+    adj_count(ctr, kAdjNone);
     return false;
-  if (use_p) {
-    const double bound = (top_p > 0.0f ? (double)top_p : 0.0) * (double)kept;
-    if (!adj_resolve<TT, NT>(row, V, vec, M, c, fscale, true, 0u, bound, pol, A, key, kept))
-      return false;
   }
   tau = key_value(key);
   S = (float)((double)kept * unscale);
@@ -917,7 +1048,9 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
   constexpr int NW = NT / 32;
   constexpr int kEl = 16 / sizeof(TT);
   __shared__ float4 red[2][NW];
-  __shared__ std::conditional_t<kAdj, AdjShared, char> adj;
+  // adjusted rows: the selection's histograms, in dynamic shared memory
+  // (sizeof(AdjShared) bytes at launch; none otherwise)
+  extern __shared__ __align__(16) unsigned char adj_smem[];
   __shared__ long long s_slot;
   __shared__ int s_gmax, s_bad, s_prefix, s_x;
   __shared__ float s_dec[4];  // px, qx, flags
@@ -1014,7 +1147,8 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
       const float pp = P.topp ? __ldg(P.topp + b) : 1.0f;
       const bool use_k = kk >= 1 && kk < V, use_p = !(pp >= 1.0f);
       if ((use_k || use_p) && M > -INFINITY && M < INFINITY)
-        adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, keep, adj, tau, S);
+        adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, keep,
+                           *reinterpret_cast<AdjShared*>(adj_smem), tau, S, P.adj_ctr);
     }
     const float invS = 1.0f / S;
 

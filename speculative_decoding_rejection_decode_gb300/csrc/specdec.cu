@@ -58,6 +58,8 @@ struct specdec_ctx {
   int stream_ctas = 1;          // stream kernel CTAs per SM (1 or 2)
   int pair_clusters[2] = {0, 0};  // co-resident 2-CTA clusters of pair_row_kernel<f32 / bf16>
   int occ_cache[2][5][2] = {};  // [dtype][cluster index] -> {smem, clusters}
+  int adj_smem_set[2] = {0, 0};  // dynamic shared memory set on the adjusted sweep kernel
+  unsigned long long* adj_ctr = nullptr;  // caller's selection counters (profiling), or null
 };
 
 namespace {
@@ -230,8 +232,17 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
     }
     kern<<<h->num_sms * ctas, kStreamThreads, smem, st>>>(P);
   } else if (path == SPECDEC_PATH_SWEEP) {
-    if (P.topk || P.topp)
-      sweep_row_kernel<TT, 512, 2, true><<<h->num_sms * 2, 512, 0, st>>>(P);
+    if (P.topk || P.topp) {
+      auto kern = sweep_row_kernel<TT, 512, 2, true>;
+      int& set = h->adj_smem_set[sizeof(TT) == 2];
+      if (!set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(AdjShared)) != cudaSuccess)
+          return SPECDEC_ERR_CUDA;
+        set = 1;
+      }
+      kern<<<h->num_sms * 2, 512, sizeof(AdjShared), st>>>(P);
+    }
     else if (h->sweep_threads == 512)
       sweep_row_kernel<TT, 512, 2><<<h->num_sms * 2, 512, 0, st>>>(P);
     else if (h->sweep_threads == 256)
@@ -366,6 +377,7 @@ int specdec_rejection_sample_topk_topp(
   P.topk = T > 0.0f ? top_k : nullptr;   // the greedy path keeps the argmax either way
   P.topp = T > 0.0f ? top_p : nullptr;
   P.row_tau = (P.topk || P.topp) ? h->ws.row_tau : nullptr;
+  P.adj_ctr = h->adj_ctr;
   P.rslices = (int)std::min<int64_t>(kRaceMaxSlices, std::max<int64_t>(1, (V + 4095) / 4096));
   P.rslice_len = (int)round_up((V + P.rslices - 1) / P.rslices, 8);
   P.defer_count = reinterpret_cast<int32_t*>(h->small + 1);
@@ -450,6 +462,12 @@ int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after
   if (!h || (before_rows == nullptr) != (after_rows == nullptr)) return SPECDEC_ERR_INVALID_ARG;
   h->ev_before = static_cast<cudaEvent_t>(before_rows);
   h->ev_after = static_cast<cudaEvent_t>(after_rows);
+  return SPECDEC_OK;
+}
+
+int specdec_set_adjust_counters(specdec_handle_t h, uint64_t* device_counters) {
+  if (!h) return SPECDEC_ERR_INVALID_ARG;
+  h->adj_ctr = reinterpret_cast<unsigned long long*>(device_counters);
   return SPECDEC_OK;
 }
 

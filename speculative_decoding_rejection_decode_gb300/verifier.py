@@ -13,7 +13,7 @@ from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_FU
                    specdec_get_error, specdec_last_path, specdec_neg_log_uniform,
                    specdec_rejection_sample, specdec_rejection_sample_ex,
                    specdec_rejection_sample_noalloc, specdec_rejection_sample_topk_topp,
-                   specdec_reserve,
+                   specdec_reserve, specdec_set_adjust_counters,
                    specdec_set_path, specdec_set_timing_events, specdec_status_string,
                    specdec_uniform)
 
@@ -84,6 +84,14 @@ class Verifier:
         a = None if before_rows is None else before_rows.cuda_event
         b = None if after_rows is None else after_rows.cuda_event
         _check(specdec_set_timing_events(self._h, a, b), "specdec_set_timing_events")
+
+    def set_adjust_counters(self, counters: torch.Tensor | None):
+        """int64 [8] device tensor that later calls add their top-k / top-p
+        selection statistics to (see specdec_set_adjust_counters); None stops."""
+        if counters is not None and (counters.device != self.device or counters.dtype != torch.int64
+                                     or counters.numel() < 8):
+            raise ValueError("counters must be an int64 tensor of 8 entries on the device")
+        _check(specdec_set_adjust_counters(self._h, _ptr(counters)), "specdec_set_adjust_counters")
 
     def set_path(self, path: int):
         _check(specdec_set_path(self._h, path), "specdec_set_path")
