@@ -41,7 +41,7 @@
  *
  * Ownership: the caller owns every input and output buffer (device memory).  The
  * handle owns a device workspace (per-row softmax statistics, adjusted-row
- * thresholds, status words and greedy keys, 28 bytes per target row, plus 268
+ * thresholds, status words and greedy keys, 28 bytes per target row, plus 1036
  * bytes per request) and
  * one stream-ordered error word.  A handle serves one stream at a time; calls on it are
  * asynchronous and never synchronise, except the first call that needs a larger

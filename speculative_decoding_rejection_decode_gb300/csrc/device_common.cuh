@@ -97,10 +97,43 @@ __device__ __forceinline__ void race_merge(Race& a, float bw, float be, int32_t 
   }
 }
 
+// Pruning that never changes the winner: E = -ln U >= 1 - U = d for every
+// U, and d >= 2^-24 here, so an entry whose key bound w / d (computed with a
+// 2^-16 margin, far above the rounding of the products) stays below the
+// current best key a.w / a.e loses to it, and neither its log nor (when even
+// d = 2^-24 cannot help) its hash is needed.
+constexpr float kRaceMargin = 1.0f - 1.0f / 65536.0f;
+__device__ __forceinline__ bool race_hopeless(const Race& a, float w, float d) {
+  return a.w > 0.0f && w * a.e < a.w * (d * kRaceMargin);
+}
+__device__ __forceinline__ float one_minus_uniform(uint32_t k) {
+  return (float)((1u << 24) - 2u * k - 1u) * (1.0f / 16777216.0f);  // exact
+}
+
+// Offers entries v .. v+3 with weights w[0..3]: the four hashes are independent
+// (no branch between them); only entries that pass the bound take the log and
+// the comparison.  Checking all four against the best from before the group is
+// conservative, so the result is the one race_offer gives one by one.
+__device__ __forceinline__ void race_offer4(Race& a, const float* w, uint64_t key, uint32_t v) {
+  uint32_t k[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) k[i] = uniform_bits(key, v + i);
+  bool c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = w[i] > 0.0f && !race_hopeless(a, w[i], one_minus_uniform(k[i]));
+  if (c[0] | c[1] | c[2] | c[3]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (c[i]) race_merge(a, w[i], neg_log_uniform(k[i]), (int32_t)(v + i));
+  }
+}
+
 // Offers vocabulary entry v with weight w (w <= 0: not a candidate).
 __device__ __forceinline__ void race_offer(Race& a, float w, uint64_t key, uint32_t v) {
-  const float e = neg_log_uniform(uniform_bits(key, v));
-  race_merge(a, w, e, (int32_t)v);
+  if (!(w > 0.0f) || race_hopeless(a, w, 1.0f / 16777216.0f)) return;
+  const uint32_t k = uniform_bits(key, v);
+  if (race_hopeless(a, w, one_minus_uniform(k))) return;
+  race_merge(a, w, neg_log_uniform(k), (int32_t)v);
 }
 
 // exp2 on the special-function unit (flush-to-zero; arguments here are <= 0).

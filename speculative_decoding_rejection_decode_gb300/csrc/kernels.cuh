@@ -56,10 +56,11 @@ struct Params {
   int32_t* ws_nacc;        // [cap_B] n_b for the race kernel
   int32_t* defer_list;     // [cap_B]
   int32_t* defer_count;    // [1]
-  float4* rpart;           // [cap_B * kRaceMaxSlices] partial race winners per deferred request
+  float4* rpart;           // [cap_B * rstride] partial race winners per deferred request
   int32_t* rcount;         // [cap_B] slices finished per deferred request (reset by the last one)
   int rslices;             // slices per deferred row
   int rslice_len;          // elements per slice (multiple of 8)
+  int rstride;             // rpart entries per deferred request (>= rslices)
   unsigned long long* sched;  // [1] next work slot of the sweep kernel (reset by finalize)
   const int32_t* topk;     // [B] per-request top-k or null (adjusted rows, sweep kernel only)
   const float* topp;       // [B] per-request top-p or null
@@ -76,7 +77,8 @@ struct Params {
 };
 
 constexpr int kChunk = 4096;          // elements per bulk copy / pipeline step
-constexpr int kRaceMaxSlices = 16;    // a deferred row is split over at most this many CTAs
+constexpr int kRaceMaxSlices = 64;    // a deferred row is split over at most this many CTAs
+constexpr int kRaceSliceTarget = 4096; // elements per slice the split aims at
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kFusedThreads = kConsumers + 32;  // + one producer warp
@@ -485,18 +487,13 @@ __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float
   if constexpr (kHasQ)
     beta += (fminf(p[0], qv[0]) + fminf(p[1], qv[1])) + (fminf(p[2], qv[2]) + fminf(p[3], qv[3]));
   if constexpr (kRace) {
-    float e[4];
-    uint32_t kb[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) kb[k] = uniform_bits(rkey, v + k);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) e[k] = neg_log_uniform(kb[k]);
+    float w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float w = (kHasQ && resid) ? fmaxf(p[k] - qv[k], 0.0f) : p[k];
-      if (!kHasQ && (int)(v + k) == excl) w = 0.0f;  // one-hot draft: residual is p without x
-      race_merge(best, w, e[k], (int32_t)(v + k));
+      w[k] = (kHasQ && resid) ? fmaxf(p[k] - qv[k], 0.0f) : p[k];
+      if (!kHasQ && (int)(v + k) == excl) w[k] = 0.0f;  // one-hot draft: residual is p without x
     }
+    race_offer4(best, w, rkey, v);
   }
 }
 
@@ -1947,16 +1944,81 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
     const int excl = (has_q && onehot) ? __ldg(P.ids + c0 + n) : -1;  // residual of a one-hot draft
     const uint64_t rkey = stream_key(P.seed, P.req_offset + b, n, 1);
     const int v0 = sl * P.rslice_len, v1 = min(V, v0 + P.rslice_len);
-    Race best = race_none();
-    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-      const float xv = load_logit(row + v);
+    // Visits the slice's (weight, index) pairs: 16-byte loads where rows are
+    // 16-byte aligned (v0 is a multiple of 8), elements otherwise.
+    auto weight = [&](float xv, float qv, int v) {
       const float p = xv >= tau ? ex2((xv - ms.x) * P.c) * invS : 0.0f;
-      const float w = qrow ? fmaxf(p - __ldg(qrow + v), 0.0f) : (v == excl ? 0.0f : p);
-      race_offer(best, w, rkey, (uint32_t)v);
+      return qrow ? fmaxf(p - qv, 0.0f) : (v == excl ? 0.0f : p);
+    };
+    // f4(w[4], v): entries v .. v+3; f1(w, v): single entries of the remainder
+    auto visit = [&](auto&& f4, auto&& f1) {
+      int vs = v0;  // start of the scalar remainder
+      if (P.vec_ok) {
+        constexpr int kEl = 16 / sizeof(TT);
+        const int n_vec = (v1 - v0) / kEl;
+        const uint4* rv = reinterpret_cast<const uint4*>(row + v0);
+        for (int j = threadIdx.x; j < n_vec; j += blockDim.x) {
+          float x[kEl];
+          unpack16<TT>(__ldg(rv + j), x);
+          const int v = v0 + j * kEl;
+#pragma unroll
+          for (int h = 0; h < kEl / 4; ++h) {
+            float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (qrow) q4 = __ldg(reinterpret_cast<const float4*>(qrow + v) + h);
+            const float w[4] = {weight(x[4 * h + 0], q4.x, v + 4 * h + 0),
+                                weight(x[4 * h + 1], q4.y, v + 4 * h + 1),
+                                weight(x[4 * h + 2], q4.z, v + 4 * h + 2),
+                                weight(x[4 * h + 3], q4.w, v + 4 * h + 3)};
+            f4(w, v + 4 * h);
+          }
+        }
+        vs = v0 + n_vec * kEl;
+      }
+      for (int v = vs + threadIdx.x; v < v1; v += blockDim.x)
+        f1(weight(load_logit(row + v), qrow ? __ldg(qrow + v) : 0.0f, v), v);
+    };
+    // Seed: the slice's heaviest entry enters the race first, so that the
+    // pruning in race_offer drops the log (and often the hash) of nearly every
+    // other entry.  Pruning never changes the winner.
+    float wmax = 0.0f;
+    int imax = 0x7FFFFFFF;
+    auto track = [&](float w, int v) {
+      if (w > wmax || (w == wmax && w > 0.0f && v < imax)) {
+        wmax = w;
+        imax = v;
+      }
+    };
+    visit([&](const float* w, int v) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) track(w[i], v + i);
+    }, track);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float w2 = __shfl_xor_sync(0xFFFFFFFFu, wmax, o);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, imax, o);
+      if (w2 > wmax || (w2 == wmax && i2 < imax)) {
+        wmax = w2;
+        imax = i2;
+      }
     }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(wmax, __int_as_float(imax), 0.f, 0.f);
+    __syncthreads();
+    Race best = race_none();
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      const float w2 = red[w].x;
+      const int i2 = __float_as_int(red[w].y);
+      if (w2 > wmax || (w2 == wmax && i2 < imax)) {
+        wmax = w2;
+        imax = i2;
+      }
+    }
+    __syncthreads();
+    if (wmax > 0.0f) race_offer(best, wmax, rkey, (uint32_t)imax);
+    visit([&](const float* w, int v) { race_offer4(best, w, rkey, (uint32_t)v); },
+          [&](float w, int v) { race_offer(best, w, rkey, (uint32_t)v); });
     const Race tb = block_race<TT>(best, red);
     if (threadIdx.x == 0) {
-      P.rpart[(int64_t)k * kRaceMaxSlices + sl] = make_float4(tb.w, tb.e, __int_as_float(tb.idx), 0.f);
+      P.rpart[(int64_t)k * P.rstride + sl] = make_float4(tb.w, tb.e, __int_as_float(tb.idx), 0.f);
       __threadfence();
       s_last = (atomicAdd(P.rcount + k, 1) == S - 1);
     }
@@ -1965,7 +2027,7 @@ __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
       __threadfence();
       Race all = race_none();
       for (int s2 = 0; s2 < S; ++s2) {
-        const float4 r = __ldcg(P.rpart + (int64_t)k * kRaceMaxSlices + s2);
+        const float4 r = __ldcg(P.rpart + (int64_t)k * P.rstride + s2);
         race_merge(all, r.x, r.y, __float_as_int(r.z));
       }
       if (!(all.w > 0.0f)) {  // empty residual: race over p instead

@@ -25,6 +25,7 @@ namespace {
 constexpr int64_t kRows = SPECDEC_NOALLOC_MAX_ROWS;
 constexpr int kBatch = SPECDEC_NOALLOC_MAX_BATCH;
 constexpr int kThreads = 512;  // sweep kernel: 2 CTAs of 512 threads per SM
+constexpr int kSlices = 16;    // race slices per deferred request (keeps the scratch small)
 
 constexpr size_t kStatsOff = 0;
 constexpr size_t kStatusOff = kStatsOff + kRows * sizeof(float2);
@@ -32,7 +33,7 @@ constexpr size_t kKeysOff = kStatusOff + kRows * sizeof(uint64_t);
 constexpr size_t kNaccOff = kKeysOff + kRows * sizeof(uint64_t);
 constexpr size_t kListOff = kNaccOff + kBatch * sizeof(int32_t);
 constexpr size_t kRpartOff = kListOff + kBatch * sizeof(int32_t);
-constexpr size_t kRcountOff = kRpartOff + (size_t)kBatch * kRaceMaxSlices * sizeof(float4);
+constexpr size_t kRcountOff = kRpartOff + (size_t)kBatch * kSlices * sizeof(float4);
 constexpr size_t kSmallOff = kRcountOff + kBatch * sizeof(int32_t);  // err, defer count, counter
 constexpr size_t kSmallBytes = 64;
 constexpr size_t kScratchBytes = kSmallOff + kSmallBytes;
@@ -119,8 +120,9 @@ extern "C" int specdec_rejection_sample_noalloc(
   P.defer_list = reinterpret_cast<int32_t*>(base + kListOff);
   P.rpart = reinterpret_cast<float4*>(base + kRpartOff);
   P.rcount = reinterpret_cast<int32_t*>(base + kRcountOff);
-  P.rslices = (int)std::min<int64_t>(kRaceMaxSlices, std::max<int64_t>(1, (V + 4095) / 4096));
+  P.rslices = (int)std::min<int64_t>(kSlices, std::max<int64_t>(1, (V + 4095) / 4096));
   P.rslice_len = (int)(((V + P.rslices - 1) / P.rslices + 7) / 8 * 8);
+  P.rstride = kSlices;
   P.err = out_device_error ? out_device_error : small;
   P.defer_count = reinterpret_cast<int32_t*>(small + 1);
   P.sched = reinterpret_cast<unsigned long long*>(small + 2);
@@ -140,7 +142,7 @@ extern "C" int specdec_rejection_sample_noalloc(
     P.vec_ok = ((int64_t)V * esize) % 16 == 0 && ((int64_t)V * 4) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
-    const int race_grid = sms * 4;
+    const int race_grid = sms * 8;
     if (dtype == SPECDEC_BF16) {
       sweep_row_kernel<__nv_bfloat16, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
       finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);

@@ -273,7 +273,7 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
   }
   if (h->ev_after) cudaEventRecord(h->ev_after, st);
   finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
-  race_kernel<TT><<<h->num_sms * 4, kRowThreads, 0, st>>>(P);
+  race_kernel<TT><<<h->num_sms * 8, kRowThreads, 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
@@ -378,8 +378,10 @@ int specdec_rejection_sample_topk_topp(
   P.topp = T > 0.0f ? top_p : nullptr;
   P.row_tau = (P.topk || P.topp) ? h->ws.row_tau : nullptr;
   P.adj_ctr = h->adj_ctr;
-  P.rslices = (int)std::min<int64_t>(kRaceMaxSlices, std::max<int64_t>(1, (V + 4095) / 4096));
+  P.rslices = (int)std::min<int64_t>(
+      kRaceMaxSlices, std::max<int64_t>(1, (V + kRaceSliceTarget - 1) / kRaceSliceTarget));
   P.rslice_len = (int)round_up((V + P.rslices - 1) / P.rslices, 8);
+  P.rstride = kRaceMaxSlices;
   P.defer_count = reinterpret_cast<int32_t*>(h->small + 1);
   P.err = h->small;
   P.cap_rows = h->ws.cap_rows;
