@@ -87,6 +87,32 @@ constexpr int kMaxChunks = 64;
 
 __device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
 
+// Kernels launched as programmatic dependents (launch_dependent below) start
+// while the previous kernel in the stream drains and wait here, before their
+// first read of its results, until it has completed and its writes are visible.
+__device__ __forceinline__ void wait_for_previous_kernel() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launches kern<<<grid, block, 0, st>>>(args...) as a programmatic dependent of
+// the previous kernel on st: its launch and block placement overlap that
+// kernel's tail; the kernel itself must call wait_for_previous_kernel() first.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), int grid, int block, cudaStream_t st,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------------------
 // Fused single-pass row kernel (T > 0).
 // ---------------------------------------------------------------------------
@@ -1871,6 +1897,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(const Params P) {
 // the list of requests whose extra token the race kernel still has to draw.
 // ---------------------------------------------------------------------------
 static __global__ void finalize_kernel(const Params P) {
+  wait_for_previous_kernel();
   const int B = P.B;
   if (blockIdx.x == 0 && threadIdx.x == 0 && P.sched) *P.sched = 0ull;
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
@@ -1925,6 +1952,7 @@ template <typename TT>
 __global__ void __launch_bounds__(kRowThreads) race_kernel(const Params P) {
   __shared__ float4 red[kRowThreads / 32];
   __shared__ int s_last;
+  wait_for_previous_kernel();
   const int V = P.V;
   const int count = *P.defer_count;
   const int S = P.rslices;
@@ -2128,6 +2156,7 @@ __global__ void __launch_bounds__(kRowThreads) greedy_partial_kernel(const Param
 // rows (lowest index on ties is built into the keys), lane 0 scans.
 static __global__ void greedy_finalize_kernel(const Params P) {
   __shared__ int s_g[8][33];
+  wait_for_previous_kernel();
   const int B = P.B, V = P.V;
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   for (int b = blockIdx.x * 8 + wib; b < B; b += gridDim.x * 8) {

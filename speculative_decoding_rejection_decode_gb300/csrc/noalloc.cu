@@ -137,21 +137,24 @@ extern "C" int specdec_rejection_sample_noalloc(
       greedy_partial_kernel<__nv_bfloat16><<<sms * 8, kRowThreads, 0, st>>>(P, vec_ok);
     else
       greedy_partial_kernel<float><<<sms * 8, kRowThreads, 0, st>>>(P, vec_ok);
-    greedy_finalize_kernel<<<(B + 7) / 8, 256, 0, st>>>(P);
+    if (launch_dependent(greedy_finalize_kernel, (B + 7) / 8, 256, st, P) != cudaSuccess)
+      return SPECDEC_ERR_CUDA;
   } else {
     P.vec_ok = ((int64_t)V * esize) % 16 == 0 && ((int64_t)V * 4) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
                reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
     const int race_grid = sms * 8;
+    cudaError_t e;
     if (dtype == SPECDEC_BF16) {
       sweep_row_kernel<__nv_bfloat16, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
-      finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
-      race_kernel<__nv_bfloat16><<<race_grid, kRowThreads, 0, st>>>(P);
+      e = launch_dependent(finalize_kernel, (B + 255) / 256, 256, st, P);
+      if (e == cudaSuccess) e = launch_dependent(race_kernel<__nv_bfloat16>, race_grid, kRowThreads, st, P);
     } else {
       sweep_row_kernel<float, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
-      finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
-      race_kernel<float><<<race_grid, kRowThreads, 0, st>>>(P);
+      e = launch_dependent(finalize_kernel, (B + 255) / 256, 256, st, P);
+      if (e == cudaSuccess) e = launch_dependent(race_kernel<float>, race_grid, kRowThreads, st, P);
     }
+    if (e != cudaSuccess) return SPECDEC_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }

@@ -272,8 +272,9 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
     verify_kernel<TT><<<grid, kRowThreads, 0, st>>>(P);
   }
   if (h->ev_after) cudaEventRecord(h->ev_after, st);
-  finalize_kernel<<<(B + 255) / 256, 256, 0, st>>>(P);
-  race_kernel<TT><<<h->num_sms * 8, kRowThreads, 0, st>>>(P);
+  if (launch_dependent(finalize_kernel, (B + 255) / 256, 256, st, P) != cudaSuccess ||
+      launch_dependent(race_kernel<TT>, h->num_sms * 8, kRowThreads, st, P) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
@@ -282,7 +283,8 @@ int launch_greedy(specdec_ctx* h, Params& P, bool vec_ok, cudaStream_t st) {
   if (h->ev_before) cudaEventRecord(h->ev_before, st);
   greedy_partial_kernel<TT><<<h->num_sms * 8, kRowThreads, 0, st>>>(P, vec_ok ? 1 : 0);
   if (h->ev_after) cudaEventRecord(h->ev_after, st);
-  greedy_finalize_kernel<<<(P.B + 7) / 8, 256, 0, st>>>(P);
+  if (launch_dependent(greedy_finalize_kernel, (P.B + 7) / 8, 256, st, P) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
