@@ -189,7 +189,8 @@ int specdec_rejection_sample_topk_topp(
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream);
 
 /* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
- * _STREAM, _PAIR or _AUTO, the default, which takes SWEEP).  A forced FUSED or STREAM
+ * _STREAM, _PAIR or _AUTO, the default, which takes PAIR for batches of fewer
+ * requests than twice the SM count and SWEEP otherwise).  A forced FUSED or STREAM
  * path falls back to SWEEP where its layout rules (16-byte aligned rows; for
  * FUSED a vocabulary that fits a cluster) do not hold. */
 int specdec_set_path(specdec_handle_t h, int path);

@@ -403,7 +403,12 @@ int specdec_rejection_sample_topk_topp(
              reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
              reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
   P.sched = reinterpret_cast<unsigned long long*>(h->small + 2);
-  int path = h->path_override == SPECDEC_PATH_AUTO ? SPECDEC_PATH_SWEEP : h->path_override;
+  // AUTO: with fewer requests than sweep CTAs (2 per SM), the sweep kernel's
+  // later rows of a request usually decide before its earlier rows finish and
+  // their races go to the race kernel; the pair kernel holds half as many rows
+  // in flight, so it keeps them ahead (and halves the rows live in L2)
+  int path = h->path_override;
+  if (path == SPECDEC_PATH_AUTO) path = B < 2 * h->num_sms ? SPECDEC_PATH_PAIR : SPECDEC_PATH_SWEEP;
   if (!draft_probs) path = SPECDEC_PATH_SWEEP;  // one-hot drafts: the sweep kernel handles them
   if (P.topk || P.topp) path = SPECDEC_PATH_SWEEP;  // so do adjusted (top-k / top-p) rows
   if (path == SPECDEC_PATH_STREAM && !P.vec_ok) path = SPECDEC_PATH_SWEEP;

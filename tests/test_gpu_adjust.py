@@ -110,7 +110,10 @@ def test_onehot_drafts_with_settings(V):
 
 
 def test_switched_off_matches_the_plain_call(V):
+    # adjusted calls run on the sweep path; compare with a plain call on that path
+    from speculative_decoding_rejection_decode_gb300 import SPECDEC_PATH_SWEEP
     w = make_config(3, device="cuda", B=40, V=20000)
+    V.set_path(SPECDEC_PATH_SWEEP)
     plain = run_gpu(V, w)
     off_k = torch.full((w.B,), 0, dtype=torch.int32)
     off_p = torch.full((w.B,), 1.0)
@@ -118,6 +121,7 @@ def test_switched_off_matches_the_plain_call(V):
         g = run_gpu_adj(V, w, tk, tp)
         for key in plain:
             assert np.array_equal(g[key], plain[key]), key
+    V.set_path(0)
 
 
 def test_top_k_one_reproduces_greedy_tokens(V):
