@@ -2101,24 +2101,28 @@ __global__ void __launch_bounds__(kRowThreads) greedy_partial_kernel(const Param
   for (int64_t it = warp_id; it < items; it += nwarps) {
     const int64_t t = it / per_row;
     const int ch = (int)(it % per_row);
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    // The chunk's loads go out first (row t < cu[B] + B exists by the layout);
+    // the request lookup (a binary search over cu) runs while they are in flight.
+    const int nv = V / kEl;
+    const int j0 = ch * kChunkVec + lane;
+    uint4 w[kPer];
+    if (vec_ok) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (j0 + 32 * k < nv) w[k] = __ldg(reinterpret_cast<const uint4*>(row) + j0 + 32 * k);
+    }
     // only rows of well-formed requests are accumulated: exactly the rows the
     // finalize kernel reads and resets
     const int b = request_of_target(P.cu, B, t);
     const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
     const int64_t t0 = (int64_t)c0 + b;
     if (g < 0 || t < t0 || t > t0 + g || t0 + g >= P.cap_rows) continue;
-    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
     // Each lane scans its elements in increasing index order, so a strict
     // "greater" keeps the lowest index on ties (and -0.0 == +0.0, as numbers).
     float bv = -INFINITY;
     int bi = -1;
     if (vec_ok) {
-      const int nv = V / kEl;
-      const int j0 = ch * kChunkVec + lane;
-      uint4 w[kPer];
-#pragma unroll
-      for (int k = 0; k < kPer; ++k)
-        if (j0 + 32 * k < nv) w[k] = __ldg(reinterpret_cast<const uint4*>(row) + j0 + 32 * k);
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
         const int j = j0 + 32 * k;
