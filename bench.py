@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--config", type=int, default=4, help="standard workload 0..4")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V")
-    ap.add_argument("--path", choices=["auto", "fused", "sweep", "stream", "pair", "two_pass"],
+    ap.add_argument("--path", choices=["auto", "fused", "sweep", "stream", "pair", "dual", "two_pass"],
                     default="auto")
     ap.add_argument("--draft", choices=["probs", "onehot"], default="probs",
                     help="onehot: no draft rows (a greedy drafter, q = one-hot at the draft id)")
@@ -297,7 +297,7 @@ def main():
     if args.path != "auto":
         v.set_path({"fused": sd.SPECDEC_PATH_FUSED, "sweep": sd.SPECDEC_PATH_SWEEP,
                     "stream": sd.SPECDEC_PATH_STREAM, "pair": sd.SPECDEC_PATH_PAIR,
-                    "two_pass": sd.SPECDEC_PATH_TWO_PASS}[args.path])
+                    "dual": sd.SPECDEC_PATH_DUAL, "two_pass": sd.SPECDEC_PATH_TWO_PASS}[args.path])
     out = sd.VerifyOutput(tokens=torch.empty(w.n_target, dtype=torch.int32, device=dev),
                           num_accepted=torch.empty(w.B, dtype=torch.int32, device=dev),
                           beta=torch.empty(w.n_draft, dtype=torch.float32, device=dev))
@@ -326,12 +326,15 @@ def main():
     path, csize = v.last_path()
     launches_per_step = {sd.SPECDEC_PATH_FUSED: 3, sd.SPECDEC_PATH_TWO_PASS: 4,
                          sd.SPECDEC_PATH_SWEEP: 3, sd.SPECDEC_PATH_STREAM: 3, sd.SPECDEC_PATH_PAIR: 3,
+                         sd.SPECDEC_PATH_DUAL: 3,
                          sd.SPECDEC_PATH_GREEDY: 2}[path]
     kernel_name = {sd.SPECDEC_PATH_FUSED: "fused_row_kernel", sd.SPECDEC_PATH_SWEEP: "sweep_row_kernel",
                    sd.SPECDEC_PATH_STREAM: "stream_row_kernel", sd.SPECDEC_PATH_PAIR: "pair_row_kernel",
+                   sd.SPECDEC_PATH_DUAL: "dual_row_kernel",
                    sd.SPECDEC_PATH_TWO_PASS: "stats_kernel+verify_kernel",
                    sd.SPECDEC_PATH_GREEDY: "greedy_partial_kernel"}[path]
-    path_name = {1: "fused", 2: "two_pass", 3: "sweep", 4: "greedy", 5: "stream", 6: "pair"}[path]
+    path_name = {1: "fused", 2: "two_pass", 3: "sweep", 4: "greedy", 5: "stream", 6: "pair",
+                 7: "dual"}[path]
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),

@@ -41,7 +41,8 @@
  *
  * Ownership: the caller owns every input and output buffer (device memory).  The
  * handle owns a device workspace (per-row softmax statistics, adjusted-row
- * thresholds, status words and greedy keys, 28 bytes per target row, plus 1036
+ * thresholds, status words, greedy keys and the dual kernel's halves, 80 bytes
+ * per target row, plus 1036
  * bytes per request) and
  * one stream-ordered error word.  A handle serves one stream at a time; calls on it are
  * asynchronous and never synchronise, except the first call that needs a larger
@@ -95,6 +96,9 @@ typedef struct specdec_ctx* specdec_handle_t;
                                    memory ring (T > 0; needs 16-byte aligned rows)   */
 #define SPECDEC_PATH_PAIR 6     /* the two sweeps with each row split over a 2-CTA
                                    cluster (T > 0)                                    */
+#define SPECDEC_PATH_DUAL 7     /* two independent CTAs per row: each sweeps the whole
+                                   row for (max, sum) and half of it for the rest;
+                                   the second to finish combines (T > 0)            */
 
 /* Creates a handle bound to CUDA device `device`.  *out receives the handle.
  * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (null out, bad device) or
@@ -189,7 +193,7 @@ int specdec_rejection_sample_topk_topp(
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream);
 
 /* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
- * _STREAM, _PAIR or _AUTO, the default, which takes PAIR for batches of fewer
+ * _STREAM, _PAIR, _DUAL or _AUTO, the default, which takes PAIR for batches of fewer
  * requests than twice the SM count and SWEEP otherwise).  A forced FUSED or STREAM
  * path falls back to SWEEP where its layout rules (16-byte aligned rows; for
  * FUSED a vocabulary that fits a cluster) do not hold. */

@@ -39,6 +39,7 @@ SPECDEC_PATH_SWEEP = 3
 SPECDEC_PATH_GREEDY = 4
 SPECDEC_PATH_STREAM = 5
 SPECDEC_PATH_PAIR = 6
+SPECDEC_PATH_DUAL = 7
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

@@ -66,6 +66,10 @@ struct Params {
   const float* topp;       // [B] per-request top-p or null
   float* row_tau;          // [cap_rows] logit threshold of each adjusted row, or null
   unsigned long long* adj_ctr;  // [kAdjCounters] selection statistics (profiling), or null
+  float4* dual_part;       // [2 cap_rows] dual kernel: each half's (beta, race w, e, index)
+  int32_t* dual_cnt;       // [cap_rows] dual kernel: halves done (0 between calls)
+  unsigned long long* dual_skip;  // [cap_rows] dual kernel: bonus-row skip decision (epoch-tagged)
+  unsigned long long* dual_race;  // [cap_rows] dual kernel: race decision (epoch-tagged)
   uint32_t* err;           // [1] sticky device error word
   int64_t cap_rows;
   int cap_b;
@@ -1242,6 +1246,209 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     }
     // s_slot / s_dec / red[par] are rewritten next iteration only after the
     // __syncthreads that follows thread 0's next slot grab.
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dual row kernel (T > 0): every row is verified by two CTAs, neither of which
+// ever waits for the other.  Each sweeps the whole target row once for (max,
+// sum) (the second read of a row is served by L2, usually while the first is
+// still in flight), so both hold bit-identical (M, S) and take the same accept
+// test; each then runs sweep 2 over its half of the row.  Decisions that
+// depend on timing (skipping a bonus row whose request already rejected,
+// drawing the race) are taken once per row by whichever CTA gets there first
+// (compare-and-swap on an epoch-tagged word); the halves' (beta, race) meet in
+// global memory and the CTA that finishes second combines them, in a fixed
+// order, and writes the row's outputs and status.  Work units are half rows
+// handed out in position-major order, so half as many rows are live between
+// their two sweeps as in the sweep kernel at the same CTA count.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kDualSkip = 1u, kDualKeep = 2u, kDualRace = 1u, kDualNoRace = 2u;
+
+// The row's decision for this call: the first caller's `want` (epoch-tagged).
+__device__ __forceinline__ uint32_t dual_decide(unsigned long long* w, uint64_t epoch,
+                                                uint32_t want) {
+  const unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(w);
+  if ((cur >> 8) == epoch) return (uint32_t)(cur & 0xFF);
+  const unsigned long long mine = (epoch << 8) | want;
+  const unsigned long long old = atomicCAS(w, cur, mine);
+  return old == cur ? want : (uint32_t)(old & 0xFF);  // else the row's other CTA decided
+}
+
+template <typename TT>
+__global__ void __launch_bounds__(512, 2) dual_row_kernel(const Params P) {
+  constexpr int NT = 512, NW = NT / 32;
+  constexpr int kEl = 16 / sizeof(TT);
+  __shared__ float4 red[2][NW];
+  __shared__ long long s_slot;
+  __shared__ int s_gmax, s_bad, s_prefix;
+  __shared__ float s_dec[4];  // px, qx, flags
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = P.B, V = P.V;
+  const bool vec = P.vec_ok != 0;
+
+  if (tid == 0) {
+    s_gmax = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  {
+    int gm = 0, bad = 0;
+    for (int b = tid; b < B; b += NT) {
+      const int g = __ldg(P.cu + b + 1) - __ldg(P.cu + b);
+      gm = max(gm, g);
+      bad |= (g < 0);
+    }
+    if (gm) atomicMax(&s_gmax, gm);
+    if (bad) atomicOr(&s_bad, 1);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tid == 0) {
+    if (s_bad || __ldg(P.cu) != 0) set_err(P.err, SPECDEC_DEVERR_BAD_CU);
+    *P.defer_count = 0;
+  }
+  const int64_t total = 2 * (int64_t)B * (s_gmax + 1);  // half-row units
+  const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+  const int nunits = vec ? V / kEl : V;
+  const int halfu = (nunits + 1) / 2;
+
+  for (int it = 0;; ++it) {
+    // ---- thread 0 takes the next half row that has work ------------------
+    if (tid == 0) {
+      long long u;
+      int prefix = kPrefixAllAccepted;
+      while (true) {
+        u = (long long)atomicAdd(P.sched, 1ull);
+        if (u >= total) break;
+        const long long r = u >> 1;
+        const int i = (int)(r / B), b = (int)(r % B);
+        const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+        if (i > g) continue;
+        const int64_t t = (int64_t)c0 + b + i;
+        if (t >= P.cap_rows) {
+          set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+          continue;
+        }
+        prefix = i > 0 ? read_prefix(P.status, t - i, i, P.epoch) : kPrefixAllAccepted;
+        if (i == g &&  // a bonus row nobody needs: both halves skip it or neither does
+            dual_decide(P.dual_skip + t, P.epoch,
+                        prefix == kPrefixRejected ? kDualSkip : kDualKeep) == kDualSkip)
+          continue;
+        break;
+      }
+      s_slot = u;
+      s_prefix = prefix;
+    }
+    __syncthreads();
+    const long long u = s_slot;
+    const int prefix = s_prefix;
+    if (u >= total) break;
+    const int half = (int)(u & 1);
+    const long long r = u >> 1;
+    const int i = (int)(r / B), b = (int)(r % B);
+    const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+    const int64_t t = (int64_t)c0 + b + i, d = (int64_t)c0 + i;
+    const bool has_q = i < g;
+    const TT* row = reinterpret_cast<const TT*>(P.logits) + t * (int64_t)V;
+    const float* qrow = has_q ? P.q + d * (int64_t)V : nullptr;
+    const int par = it & 1;
+
+    int x = -1;
+    float lx = 0.0f, qx = 0.0f;
+    bool valid = true;
+    if (tid == 0 && has_q) {
+      x = __ldg(P.ids + d);
+      valid = (x >= 0 && x < V);
+      if (valid) {
+        lx = load_logit(row + x);
+        qx = __ldg(qrow + x);
+      }
+    }
+
+    // ---- sweep 1 over the whole row --------------------------------------
+    float m0, s0;
+    sweep1<TT, NT>(row, 0, nunits, vec, P.c, keep, m0, s0);
+    warp_softmax(m0, s0, P.c);
+    if (lane == 0) red[par][warp] = make_float4(m0, s0, 0.f, 0.f);
+    __syncthreads();
+    float M = -INFINITY, S = 0.0f;
+    for (int w = 0; w < NW; ++w) softmax_merge(M, S, red[par][w].x, red[par][w].y, P.c);
+    const float invS = 1.0f / S;
+
+    // ---- accept test (the same in both CTAs) and the row's race decision --
+    if (tid == 0) {
+      float px = 0.0f;
+      bool acc = false;
+      if (has_q) {
+        if (valid) px = ex2((lx - M) * P.c) * invS;
+        const float rr = uniform_from_bits(uniform_bits(stream_key(P.seed, P.req_offset + b, i, 0), 0));
+        acc = accept_test(rr, px, qx);
+      }
+      const int pfx = (prefix == kPrefixUnknown) ? read_prefix(P.status, t - i, i, P.epoch) : prefix;
+      const bool want = (pfx == kPrefixAllAccepted) && (!has_q || !acc);
+      const bool race = dual_decide(P.dual_race + t, P.epoch, want ? kDualRace : kDualNoRace) ==
+                        kDualRace;
+      s_dec[0] = px;
+      s_dec[1] = qx;
+      s_dec[2] = __int_as_float((acc ? 1 : 0) | (race ? 2 : 0) | (valid ? 0 : 4));
+    }
+    __syncthreads();
+    const int flags = __float_as_int(s_dec[2]);
+    const bool acc = flags & 1, race = flags & 2;
+    const bool resid = has_q && !acc;
+    const uint64_t rkey = stream_key(P.seed, P.req_offset + b, i, 1);
+
+    // ---- sweep 2 over this CTA's half ---------------------------------------
+    const int lo = half ? halfu : 0, hi = half ? nunits : halfu;
+    float beta = 0.0f;
+    Race best = race_none();
+    if (has_q && race)
+      sweep2<TT, NT, true, true>(row, qrow, lo, hi, vec, M, P.c, invS, -INFINITY, resid, rkey, drop,
+                                 beta, best);
+    else if (has_q)
+      sweep2<TT, NT, true, false>(row, qrow, lo, hi, vec, M, P.c, invS, -INFINITY, resid, rkey,
+                                  drop, beta, best);
+    else if (race)
+      sweep2<TT, NT, false, true>(row, qrow, lo, hi, vec, M, P.c, invS, -INFINITY, resid, rkey,
+                                  drop, beta, best);
+    beta = warp_sum(beta);
+    warp_race(best);
+    if (lane == 0) red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
+    __syncthreads();
+    if (tid == 0) {
+      float bh = 0.0f;
+      Race rh = race_none();
+      for (int w = 0; w < NW; ++w) {
+        const float4 r4 = red[par ^ 1][w];
+        bh += r4.x;
+        race_merge(rh, r4.y, r4.z, __float_as_int(r4.w));
+      }
+      P.dual_part[2 * t + half] = make_float4(bh, rh.w, rh.e, __int_as_float(rh.idx));
+      __threadfence();
+      if (atomicAdd(P.dual_cnt + t, 1) == 1) {  // second half done: combine
+        __threadfence();
+        const float4 h0 = __ldcg(P.dual_part + 2 * t), h1 = __ldcg(P.dual_part + 2 * t + 1);
+        Race tb = race_none();
+        race_merge(tb, h0.y, h0.z, __float_as_int(h0.w));
+        race_merge(tb, h1.y, h1.z, __float_as_int(h1.w));
+        P.row_stats[t] = make_float2(M, S);
+        uint32_t st = kStDone;
+        if (has_q) {
+          if (flags & 4) set_err(P.err, SPECDEC_DEVERR_BAD_DRAFT_ID);
+          if (acc) st |= kStAccepted;
+          if (P.out_beta) P.out_beta[d] = h0.x + h1.x;
+          if (P.out_px) P.out_px[d] = s_dec[0];
+          if (P.out_qx) P.out_qx[d] = s_dec[1];
+          if (P.out_acc) P.out_acc[d] = acc ? 1 : 0;
+        }
+        if (race && tb.w > 0.0f) {
+          P.out_tokens[t] = tb.idx;
+          st |= kStRaceDone;
+        }
+        P.dual_cnt[t] = 0;  // ready for the next call
+        st_relaxed_u64(P.status + t, make_status(P.epoch, st));
+      }
+    }
   }
 }
 

@@ -29,6 +29,10 @@ struct Workspace {
   int32_t* defer_list = nullptr;
   float4* rpart = nullptr;
   int32_t* rcount = nullptr;
+  float4* dual_part = nullptr;
+  int32_t* dual_cnt = nullptr;
+  unsigned long long* dual_skip = nullptr;
+  unsigned long long* dual_race = nullptr;
 };
 
 struct FusedConfig {
@@ -85,7 +89,11 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   const size_t list_b = nacc_b;
   const size_t rpart_b = round_up((size_t)b * kRaceMaxSlices * sizeof(float4), 256);
   const size_t rcount_b = nacc_b;
-  const size_t total = stats_b + tau_b + status_b + gkeys_b + nacc_b + list_b + rpart_b + rcount_b;
+  const size_t dpart_b = round_up(rows * 2 * sizeof(float4), 256);
+  const size_t dcnt_b = round_up(rows * sizeof(int32_t), 256);
+  const size_t ddec_b = round_up(rows * sizeof(unsigned long long), 256);
+  const size_t total = stats_b + tau_b + status_b + gkeys_b + nacc_b + list_b + rpart_b + rcount_b +
+                       dpart_b + dcnt_b + 2 * ddec_b;
   if (cudaDeviceSynchronize() != cudaSuccess) return SPECDEC_ERR_CUDA;
   free_workspace(h);
   void* p = nullptr;
@@ -111,6 +119,14 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
   h->ws.rpart = reinterpret_cast<float4*>(c);
   c += rpart_b;
   h->ws.rcount = reinterpret_cast<int32_t*>(c);
+  c += rcount_b;
+  h->ws.dual_part = reinterpret_cast<float4*>(c);
+  c += dpart_b;
+  h->ws.dual_cnt = reinterpret_cast<int32_t*>(c);
+  c += dcnt_b;
+  h->ws.dual_skip = reinterpret_cast<unsigned long long*>(c);
+  c += ddec_b;
+  h->ws.dual_race = reinterpret_cast<unsigned long long*>(c);
   h->ws.cap_rows = rows;
   h->ws.cap_b = b;
   return SPECDEC_OK;
@@ -231,6 +247,8 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
       cached = smem;
     }
     kern<<<h->num_sms * ctas, kStreamThreads, smem, st>>>(P);
+  } else if (path == SPECDEC_PATH_DUAL) {
+    dual_row_kernel<TT><<<h->num_sms * 2, 512, 0, st>>>(P);
   } else if (path == SPECDEC_PATH_SWEEP) {
     if (P.topk || P.topp) {
       auto kern = sweep_row_kernel<TT, 512, 2, true>;
@@ -376,6 +394,10 @@ int specdec_rejection_sample_topk_topp(
   P.defer_list = h->ws.defer_list;
   P.rpart = h->ws.rpart;
   P.rcount = h->ws.rcount;
+  P.dual_part = h->ws.dual_part;
+  P.dual_cnt = h->ws.dual_cnt;
+  P.dual_skip = h->ws.dual_skip;
+  P.dual_race = h->ws.dual_race;
   P.topk = T > 0.0f ? top_k : nullptr;   // the greedy path keeps the argmax either way
   P.topp = T > 0.0f ? top_p : nullptr;
   P.row_tau = (P.topk || P.topp) ? h->ws.row_tau : nullptr;
@@ -461,7 +483,7 @@ int specdec_get_error(specdec_handle_t h, int* device_error, void* stream) {
 }
 
 int specdec_set_path(specdec_handle_t h, int path) {
-  if (!h || path < SPECDEC_PATH_AUTO || path > SPECDEC_PATH_PAIR || path == SPECDEC_PATH_GREEDY)
+  if (!h || path < SPECDEC_PATH_AUTO || path > SPECDEC_PATH_DUAL || path == SPECDEC_PATH_GREEDY)
     return SPECDEC_ERR_INVALID_ARG;
   h->path_override = path;
   return SPECDEC_OK;

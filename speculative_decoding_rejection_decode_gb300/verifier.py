@@ -7,8 +7,8 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_FUSED,  # noqa: F401
-                   SPECDEC_PATH_GREEDY, SPECDEC_PATH_PAIR, SPECDEC_PATH_STREAM, SPECDEC_PATH_SWEEP,
+from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_DUAL,  # noqa: F401
+                   SPECDEC_PATH_FUSED, SPECDEC_PATH_GREEDY, SPECDEC_PATH_PAIR, SPECDEC_PATH_STREAM, SPECDEC_PATH_SWEEP,
                    SPECDEC_PATH_TWO_PASS, specdec_create, specdec_destroy,
                    specdec_get_error, specdec_last_path, specdec_neg_log_uniform,
                    specdec_rejection_sample, specdec_rejection_sample_ex,

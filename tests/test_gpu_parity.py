@@ -30,14 +30,15 @@ def V():
 
 
 def _paths():
-    from speculative_decoding_rejection_decode_gb300 import (SPECDEC_PATH_FUSED, SPECDEC_PATH_PAIR,
-                                                             SPECDEC_PATH_STREAM, SPECDEC_PATH_SWEEP,
+    from speculative_decoding_rejection_decode_gb300 import (SPECDEC_PATH_DUAL, SPECDEC_PATH_FUSED,
+                                                             SPECDEC_PATH_PAIR, SPECDEC_PATH_STREAM,
+                                                             SPECDEC_PATH_SWEEP,
                                                              SPECDEC_PATH_TWO_PASS)
     return {"fused": SPECDEC_PATH_FUSED, "sweep": SPECDEC_PATH_SWEEP, "stream": SPECDEC_PATH_STREAM,
-            "pair": SPECDEC_PATH_PAIR, "two_pass": SPECDEC_PATH_TWO_PASS}
+            "pair": SPECDEC_PATH_PAIR, "dual": SPECDEC_PATH_DUAL, "two_pass": SPECDEC_PATH_TWO_PASS}
 
 
-ALL_PATHS = ["pair", "stream", "fused", "sweep", "two_pass"]
+ALL_PATHS = ["dual", "pair", "stream", "fused", "sweep", "two_pass"]
 
 
 # --------------------------------------------------------------------------
