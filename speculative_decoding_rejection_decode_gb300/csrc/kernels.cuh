@@ -544,7 +544,13 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
     const uint4* qv = reinterpret_cast<const uint4*>(qrow);
     const int nv = hi;
     int j = lo + tid;
+    int round = 0;
     for (; j + (U - 1) * NT < nv; j += U * NT) {
+      if constexpr (kRace) {
+        // every few rounds each lane takes the warp's best so far, so the
+        // pruning bound tightens early (any entry already offered is a valid best)
+        if ((++round & 3) == 0) warp_race(best);
+      }
       uint4 a[U];
       uint4 b[U][kEl / 4];
 #pragma unroll
