@@ -205,7 +205,8 @@ int specdec_set_path(specdec_handle_t h, int path);
  * Pass NULL, NULL to stop.  The events stay owned by the caller. */
 int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after_rows);
 
-/* Profiling hook for adjusted (top-k / top-p) rows: when set, every later call
+/* Profiling hook for adjusted (top-k / top-p) rows (no counterpart in the pages;
+ * it reports how this library's selection resolved each row): when set, every later call
  * adds to device_counters (device memory, 8 uint64 entries, owned by the
  * caller, zeroed by the caller): [0] adjusted rows, [1] rows whose sampled
  * estimate put the edge in the tail, [2] rows whose edge lay past the
