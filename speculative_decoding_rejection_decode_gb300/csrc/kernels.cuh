@@ -545,7 +545,11 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
     const int nv = hi;
     int j = lo + tid;
     int round = 0;
-    for (; j + (U - 1) * NT < nv; j += U * NT) {
+    // With the race the loop shuffles across the warp, so it runs only while
+    // every lane of the warp (j = jw .. jw + 31) has a full step: j + lag is the
+    // warp's last j.  What is left goes through the one-vector loop below.
+    const int lag = kRace ? 31 - (tid & 31) : 0;
+    for (; j + lag + (U - 1) * NT < nv; j += U * NT) {
       if constexpr (kRace) {
         // every few rounds each lane takes the warp's best so far, so the
         // pruning bound tightens early (any entry already offered is a valid best)
