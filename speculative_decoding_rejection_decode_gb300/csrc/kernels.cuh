@@ -1,19 +1,27 @@
 // Verifier kernels.
 //
-//   fused_row_kernel   one HBM pass per (target row, draft row) pair.  A cluster
-//                      of C CTAs holds the target row in shared memory (bulk
-//                      copies), reduces (max, sum) across the cluster through
-//                      distributed shared memory, then streams the draft row once
-//                      for beta = sum min(p, q), the accept test and, when this
-//                      row is the request's first rejection (or its bonus row after
-//                      all drafts were accepted), the exponential race that draws
-//                      the extra token.
-//   stats_kernel +     the two-pass form for layouts the bulk copies cannot take
-//   verify_kernel      (unaligned rows) or vocabularies too large for a cluster.
+//   sweep_row_kernel   the default row kernel (T > 0): persistent, 2 CTAs of 512
+//                      threads per SM, one target row per CTA at a time.  Sweep 1
+//                      streams the target row from HBM for (max, sum); sweep 2
+//                      re-reads it from L2 with the draft row for beta, the accept
+//                      test and, when the request's earlier rows are known to be
+//                      accepted, the exponential race of the extra token.  With
+//                      kAdj, requests may carry top-k / top-p: a threshold
+//                      selection runs between the sweeps (the adjusted-row section).
+//   pair_row_kernel    the same sweeps with each row split over a 2-CTA cluster
+//                      ((max, sum) and partials exchanged in distributed shared
+//                      memory); the default for small batches.
+//   dual_row_kernel    two independent CTAs per row (each sweeps the whole row for
+//                      (max, sum) and half of it for the rest), no waiting.
+//   stream_row_kernel  the sweeps fed by bulk copies through a shared-memory ring.
+//   fused_row_kernel   one HBM pass per (target row, draft row) pair: a cluster of
+//                      C CTAs holds the target row in shared memory.
+//   stats_kernel +     the two-pass form, for any layout.
+//   verify_kernel
 //   finalize_kernel    per-request first-rejection scan over cu_num_draft_tokens.
 //   race_kernel        the race for requests whose extra token the row kernel could
 //                      not draw (its row ran before the earlier rows of the request
-//                      finished): re-reads that single row.
+//                      finished): re-reads that single row, in slices.
 //   greedy_*           T = 0: argmax per row (warp items, 64-bit atomicMax), then
 //                      the scan.
 //
