@@ -176,3 +176,48 @@ def test_argument_checks(V):
         run_gpu_adj(V, w, torch.zeros(w.B + 1, dtype=torch.int32), None)
     with pytest.raises(ValueError):
         run_gpu_adj(V, w, None, torch.ones(w.B, dtype=torch.float64))
+
+
+def test_greedy_ignores_settings(V):
+    # at T = 0 the argmax is always kept, so top-k / top-p change nothing
+    w = make_config(2, device="cuda", B=16, V=20000)
+    plain = run_gpu(V, w)
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=11)
+    g = run_gpu_adj(V, w, tk, tp)
+    for key in plain:
+        assert np.array_equal(g[key], plain[key]), key
+
+
+def test_request_offset_shards_reproduce_the_whole_batch(V):
+    # the generator index of request b is request_offset + b, with settings too
+    from speculative_decoding_rejection_decode_gb300.sharding import shard_workload
+    w = make_config(3, device="cuda", B=24, V=12000)
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=13)
+    whole = run_gpu_adj(V, w, tk, tp, extended=False)
+    cu = w.cu.cpu().numpy()
+    for rank in range(2):
+        sub, b0 = shard_workload(w, 2, rank)
+        b1 = b0 + sub.B
+        out = V(sub.target_logits, sub.draft_probs, sub.draft_ids, sub.cu, sub.T, sub.seed,
+                n_draft=sub.n_draft, request_offset=b0, top_k=tk[b0:b1].cuda(),
+                top_p=tp[b0:b1].cuda())
+        torch.cuda.synchronize()
+        t0, t1 = cu[b0] + b0, cu[b1] + b1
+        assert np.array_equal(out.tokens.cpu().numpy(), whole["tokens"][t0:t1])
+        assert np.array_equal(out.num_accepted.cpu().numpy(), whole["num_accepted"][b0:b1])
+
+
+def test_selection_counters(V):
+    w = make_config(1, device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=0, top_k=50, top_p=0.9)
+    ctr = torch.zeros(8, dtype=torch.int64, device="cuda")
+    V.set_adjust_counters(ctr)
+    run_gpu_adj(V, w, tk, tp)
+    V.set_adjust_counters(None)
+    c = ctr.cpu().tolist()
+    # every row that was verified was adjusted; none lacked a threshold
+    assert c[0] >= w.B and c[0] <= w.n_target
+    assert c[4] == 0
+    before = list(c)
+    run_gpu_adj(V, w, tk, tp)          # counters off: unchanged
+    assert ctr.cpu().tolist() == before
