@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--adjust-mix", action="store_true",
                     help="a seeded per-request mix of top-k / top-p settings")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="threads of the all-cores oracle rate (0: every usable core; 1: skip it)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -221,6 +223,71 @@ def oracle_sample_rate(w, seconds: float, start_request: int = 0, top_k=None, to
         done_pos += int(d1 - d0)
         b += 1
     return done_pos / elapsed, done_req, done_pos, elapsed
+
+
+def oracle_threaded_rate(w, seconds: float, threads: int, top_k=None, top_p=None):
+    """The same oracle call on `threads` host threads, each over its own
+    contiguous range of requests (the oracle's C calls release the GIL).  Each
+    thread stops after about `seconds` of oracle time or at the end of its range.
+    Returns (positions/s over the slowest thread's oracle time, requests done,
+    positions done, that time)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from speculative_decoding_rejection_decode_gb300.inputs import to_numpy_logits
+    from speculative_decoding_rejection_decode_gb300.sharding import shard_bounds
+    oracle.build()
+    oracle.pow2_neg(1.0)          # loads the library once, before the threads start
+    cu = w.cu.cpu().numpy().astype("int64")
+    tk = None if top_k is None else top_k.cpu().numpy()
+    tp = None if top_p is None else top_p.cpu().numpy()
+
+    def work(r):
+        b0, b1 = shard_bounds(w.B, threads, r)
+        nreq = npos = 0
+        el = 0.0
+        for b in range(b0, b1):
+            if el >= seconds:
+                break
+            d0, d1 = cu[b], cu[b + 1]
+            tgt = to_numpy_logits(w.target_logits[d0 + b:d1 + b + 1])
+            q = None if w.draft_probs is None else w.draft_probs[d0:d1].cpu().numpy()
+            ids = w.draft_ids[d0:d1].cpu().numpy()
+            t0 = time.perf_counter()
+            oracle.verify_request(int(b), tgt, q, ids, w.T, w.seed,
+                                  top_k=0 if tk is None else int(tk[b]),
+                                  top_p=1.0 if tp is None else float(tp[b]))
+            el += time.perf_counter() - t0
+            nreq += 1
+            npos += int(d1 - d0)
+        return nreq, npos, el
+
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        parts = list(pool.map(work, range(threads)))
+    nreq = sum(p[0] for p in parts)
+    npos = sum(p[1] for p in parts)
+    slowest = max(p[2] for p in parts)
+    return npos / max(slowest, 1e-12), nreq, npos, slowest
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo, else lscpu), or the
+    machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return f"{platform.machine()} {line.split(':', 1)[1].strip()}"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
 
 
 def adjust_settings(w, args, device):
@@ -424,10 +491,23 @@ def main():
         result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         rate, nreq, npos, el = oracle_sample_rate(w, args.cpu_seconds, top_k=tk, top_p=tp)
+        cpu = host_cpu_model()
         result["cpu_baseline"] = {
             "value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {nreq} requests ({npos} draft positions) of the same workload, "
-                      f"one thread, {el:.1f} s of oracle time"}
+                      f"one thread, {el:.1f} s of oracle time",
+            "cpu": cpu}
+        if args.cpu_threads != 1:
+            nthr = args.cpu_threads or len(os.sched_getaffinity(0))
+            rate_n, nreq_n, npos_n, el_n = oracle_threaded_rate(w, args.cpu_seconds / 3, nthr,
+                                                                top_k=tk, top_p=tp)
+            result["cpu_baseline_all_cores"] = {
+                "value": rate_n, "unit": UNIT, "cores": nthr,
+                "kind": f"oracle, {nthr} threads over requests",
+                "sample": f"{nreq_n} requests ({npos_n} draft positions) of the same workload in "
+                          f"{nthr} contiguous request ranges; rate over the slowest thread's "
+                          f"{el_n:.1f} s of oracle time",
+                "cpu": cpu}
     if dist.rank == 0:
         print(json.dumps(result), flush=True)
     v.close()
