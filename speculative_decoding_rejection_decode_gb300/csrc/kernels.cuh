@@ -768,26 +768,26 @@ __device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64
   constexpr int kStep = kSampled ? kAdjSample : 1;
   const int tid = threadIdx.x;
   if (vec) {
+    // one copy of the per-vector body (f is inlined kEl times, not 3 kEl): the
+    // next vector's load is issued before the current one is processed
     const uint4* rv = reinterpret_cast<const uint4*>(row);
     const int nv = V / kEl;
     int j = tid * kStep;
-    for (; j + NT * kStep < nv; j += 2 * NT * kStep) {
-      uint4 a[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) a[u] = ldg_hint(rv + j + u * NT * kStep, pol);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
+    if (j < nv) {
+      uint4 cur = ldg_hint(rv + j, pol);
+#pragma unroll 1
+      for (;;) {
+        const int jn = j + NT * kStep;
+        uint4 nxt = cur;
+        if (jn < nv) nxt = ldg_hint(rv + jn, pol);
         float x[kEl];
-        unpack16<TT>(a[u], x);
+        unpack16<TT>(cur, x);
 #pragma unroll
         for (int e = 0; e < kEl; ++e) f(x[e]);
+        if (jn >= nv) break;
+        cur = nxt;
+        j = jn;
       }
-    }
-    for (; j < nv; j += NT * kStep) {
-      float x[kEl];
-      unpack16<TT>(ldg_hint(rv + j, pol), x);
-#pragma unroll
-      for (int e = 0; e < kEl; ++e) f(x[e]);
     }
   } else {
     for (int v = tid * kStep; v < V; v += NT * kStep) f(load_logit(row + v));
