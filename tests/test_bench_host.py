@@ -1,0 +1,99 @@
+"""Host logic of bench.py on CPU: the all-cores oracle rate covers every request
+once, the clock sampler's parsing and throttle flags, the committed DRAM-traffic
+record's validity checks and the top-k / top-p settings of the adjusted lines."""
+import argparse
+import os
+
+import pytest
+import torch
+
+import bench
+from speculative_decoding_rejection_decode_gb300.inputs import make_config
+
+
+@pytest.mark.parametrize("threads", [1, 3, 12])
+def test_threaded_oracle_rate_covers_every_request_once(threads):
+    w = make_config(1)            # B=8, gamma=5, V=32000
+    rate, nreq, npos, slowest = bench.oracle_threaded_rate(w, 600.0, threads)
+    assert nreq == w.B and npos == w.n_draft
+    assert rate > 0 and slowest > 0
+
+
+def test_threaded_oracle_rate_with_top_k_top_p():
+    w = make_config(1)
+    tk = torch.full((w.B,), 5, dtype=torch.int32)
+    tp = torch.full((w.B,), 0.8)
+    _, nreq, npos, _ = bench.oracle_threaded_rate(w, 600.0, 4, top_k=tk, top_p=tp)
+    assert nreq == w.B and npos == w.n_draft
+
+
+def test_host_cpu_model_is_named():
+    assert isinstance(bench.host_cpu_model(), str) and bench.host_cpu_model()
+
+
+class _Done:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler_with(tmp_path, lines):
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "clocks.csv")
+    with open(s.path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    s.proc = _Done()
+    s.fh = open(tmp_path / "unused.csv", "w")
+    return s
+
+
+def test_clock_sampler_median_and_reasons(tmp_path):
+    idle = "0, 2070, 2070, 300.5, 0x0, Not Active, Not Active, Not Active, Not Active"
+    capped = "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active"
+    hot = "0, 1500, 2070, 1400.0, 0x40, Not Active, Active, Not Active, Not Active"
+    r = _sampler_with(tmp_path, [idle, capped, idle, "garbage line"]).stop()
+    assert r["sm_mhz"] == 2070 and r["sm_max_mhz"] == 2070 and r["samples"] == 3
+    assert r["reasons"] == ["sw_power_cap"] and r["power_w_max"] == 1390.0
+    r = _sampler_with(tmp_path, [idle, hot, hot]).stop()
+    assert r["sm_mhz"] == 1500 and r["reasons"] == ["hw_thermal_slowdown"]
+    r = _sampler_with(tmp_path, ["not,a,sample"]).stop()
+    assert r["samples"] == 0 and r["sm_mhz"] is None
+
+
+def test_recorded_traffic_needs_current_source_and_workload(tmp_path, monkeypatch):
+    path = tmp_path / "traffic.txt"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.recorded_traffic("w", "k") is None          # no record
+    h = bench.kernel_source_hash()
+    path.write_text("# note: a comment with a colon\n"
+                    f"kernel: k\nworkload_key: w\nsource_sha256_16: {h}\n"
+                    "traffic_bytes_per_launch: 123456\n")
+    assert bench.recorded_traffic("w", "k") == 123456.0
+    assert bench.recorded_traffic("other", "k") is None
+    assert bench.recorded_traffic("w", "other") is None
+    path.write_text(path.read_text().replace(h, "0" * 16))
+    assert bench.recorded_traffic("w", "k") is None          # taken on other kernel code
+
+
+def _args(**kw):
+    base = dict(top_k=None, top_p=None, adjust_mix=False, config=4)
+    base.update(kw)
+    return argparse.Namespace(**base)
+
+
+def test_adjust_settings():
+    w = make_config(1)
+    assert bench.adjust_settings(w, _args(), "cpu") == (None, None)
+    assert bench.adjust_desc(_args()) is None
+    tk, tp = bench.adjust_settings(w, _args(top_k=50), "cpu")
+    assert tk.dtype == torch.int32 and tk.shape == (w.B,) and bool((tk == 50).all())
+    assert tp is None or bool((tp == 1.0).all())
+    tk, tp = bench.adjust_settings(w, _args(top_p=0.9), "cpu")
+    assert tp.dtype == torch.float32 and bool((tp == torch.tensor(0.9)).all())
+    assert bench.adjust_desc(_args(top_k=50, top_p=0.9)) == {"top_k": 50, "top_p": 0.9}
+    tk1, tp1 = bench.adjust_settings(w, _args(adjust_mix=True), "cpu")
+    tk2, tp2 = bench.adjust_settings(w, _args(adjust_mix=True), "cpu")
+    assert torch.equal(tk1, tk2) and torch.equal(tp1, tp2)     # seeded
+    assert bench.adjust_desc(_args(adjust_mix=True)) == "seeded per-request mix"
