@@ -230,6 +230,21 @@ int specdec_uniform(uint64_t seed, uint64_t b, uint64_t pos, uint32_t stream_id,
  * race uses (so tests can bound its error against double precision). */
 int specdec_neg_log_uniform(uint32_t k0, int64_t n, float* out, void* stream);
 
+/* Diagnostic for the top-p edge (no counterpart in the pages; it exposes this
+ * library's float32 mass definition so that tests can compare it with an
+ * independent implementation): for j < n, out_pow2[j] = 2^-z[j] as the
+ * selection computes it (0 for z >= 64 or NaN; otherwise the degree-8 Taylor
+ * series of 2^-frac(z) with float32 coefficients (-ln 2)^i / i!, Horner's rule
+ * with fused multiply-adds, times 2^-floor(z)) and out_mass[j] = that value
+ * times 2^F, F = 62 - ceil(log2 V), rounded to the nearest integer (ties to
+ * even): the integer mass an entry at distance z (in base-2 units, z >= 0)
+ * from the maximum of a row of V entries contributes to the top-p sums.  z,
+ * out_mass and out_pow2 are device arrays of n entries; either output may be
+ * NULL.  Asynchronous on `stream`.  SPECDEC_ERR_INVALID_ARG for n < 0,
+ * V outside [1, 2^30], or n > 0 with z NULL or both outputs NULL. */
+int specdec_selection_mass(const float* z, int64_t n, int V, uint64_t* out_mass, float* out_pow2,
+                           void* stream);
+
 /* ---- allocation-free variant -----------------------------------------------
  * No counterpart in the paper: this entry point exists for callers that cannot
  * allocate device memory at the point where they verify (code running inside a

@@ -85,6 +85,8 @@ def _load():
                                                     u64, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_pow2_neg.argtypes = [ctypes.c_float]
         lib.oracle_pow2_neg.restype = ctypes.c_float
+        lib.oracle_selection_mass.argtypes = [vp, i64, i32, vp, vp]
+        lib.oracle_selection_mass.restype = None
         lib.oracle_rejection_sample_adj.restype = i32
         lib.oracle_adjusted_probs.argtypes = [vp, i32, i32, dbl, i32, dbl, vp]
         lib.oracle_adjusted_probs.restype = i32
@@ -218,6 +220,17 @@ def verify_request(b: int, target_rows: np.ndarray, draft_rows: np.ndarray | Non
 def pow2_neg(z: float) -> float:
     """2^-z on the float32 definition the top-p edge is decided with."""
     return float(_load().oracle_pow2_neg(float(z)))
+
+
+def selection_mass(z: np.ndarray, V: int) -> tuple[np.ndarray, np.ndarray]:
+    """Integer masses (uint64) and 2^-z (float32) of entries at float32
+    distances z from the maximum of a row of V entries, on the definition the
+    top-p edge is decided with."""
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    mass = np.empty(z.shape[0], np.uint64)
+    p2 = np.empty(z.shape[0], np.float32)
+    _load().oracle_selection_mass(_ptr(z), z.shape[0], int(V), _ptr(mass), _ptr(p2))
+    return mass, p2
 
 
 def adjusted_probs(row: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0,

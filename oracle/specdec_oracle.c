@@ -220,6 +220,20 @@ static int mass_shift(int V) {
   return 62 - lg;
 }
 
+/* Exported for the tests: for j < n, the integer mass of an entry at distance
+ * z[j] from the maximum of a row of V entries (as the top-p sums take it) into
+ * mass[j], and 2^-z[j] into p2[j]. */
+void oracle_selection_mass(const float* z, int64_t n, int V, uint64_t* mass, float* p2) {
+  float a[9];
+  pow2_neg_coefficients(a);
+  const int F = mass_shift(V);
+  for (int64_t j = 0; j < n; ++j) {
+    const float q = pow2_neg(z[j], a);
+    p2[j] = q;
+    mass[j] = (uint64_t)nearbyintf(ldexpf(q, F));
+  }
+}
+
 /*
  * The target distribution of one row after temperature, top-k and top-p (the
  * adjusted p of [P4] Section 2.2; the kept sets are defined in the header

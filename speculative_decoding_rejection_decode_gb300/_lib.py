@@ -74,6 +74,7 @@ _last_path = _fn("specdec_last_path", _i32, _vp, ctypes.POINTER(_i32), ctypes.PO
 _set_adj_ctr = _fn("specdec_set_adjust_counters", _i32, _vp, _vp)
 _uniform = _fn("specdec_uniform", _i32, _u64, _u64, _u64, _u32, _u64, _i64, _vp, _vp)
 _neg_log = _fn("specdec_neg_log_uniform", _i32, _u32, _i64, _vp, _vp)
+_sel_mass = _fn("specdec_selection_mass", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
 _rs_noalloc = _fn("specdec_rejection_sample_noalloc", _i32, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
                   _f32, _u64, _i64, _vp, _vp, _vp, _vp, _vp)
 _status_string = _fn("specdec_status_string", ctypes.c_char_p, _i32)
@@ -146,6 +147,10 @@ def specdec_neg_log_uniform(k0, n, out, stream) -> int:
     return _neg_log(k0, n, out, stream)
 
 
+def specdec_selection_mass(z, n, V, out_mass, out_pow2, stream) -> int:
+    return _sel_mass(z, n, V, out_mass, out_pow2, stream)
+
+
 def specdec_rejection_sample_noalloc(target_logits, dtype, draft_probs, draft_ids,
                                      cu_num_draft_tokens, B, V, T, seed, n_draft_positions,
                                      out_tokens, out_num_accepted, out_beta, out_device_error,
@@ -168,4 +173,4 @@ EXPORTED = ["specdec_create", "specdec_reserve", "specdec_rejection_sample",
             "specdec_get_error", "specdec_set_path",
             "specdec_set_timing_events", "specdec_set_adjust_counters",
             "specdec_last_path", "specdec_uniform", "specdec_neg_log_uniform",
-            "specdec_rejection_sample_noalloc", "specdec_status_string", "specdec_destroy"]
+            "specdec_selection_mass", "specdec_rejection_sample_noalloc", "specdec_status_string", "specdec_destroy"]

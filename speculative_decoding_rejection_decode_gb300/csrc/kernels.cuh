@@ -732,6 +732,18 @@ __device__ __forceinline__ float pow2_neg(float z) {
   return q * __int_as_float((127 - k) << 23);  // exact: q >= 1/2, k <= 63
 }
 
+// Integer masses of a row of V entries are pow2_neg(z) scaled by 2^F,
+// F = 62 - ceil(log2 V), so that a whole row's masses sum below 2^62; each is
+// rounded to the nearest integer (ties to even).
+__device__ __forceinline__ int adj_mass_shift(int V) {
+  const int lg = V > 1 ? 32 - __clz(V - 1) : 0;
+  return 62 - lg;
+}
+__device__ __forceinline__ float adj_mass_scale(int F) { return __int_as_float((127 + F) << 23); }
+__device__ __forceinline__ unsigned long long adj_mass(float z, float fscale) {
+  return __float2ull_rn(pow2_neg(z) * fscale);
+}
+
 // Order-preserving key of a logit (-0.0 folded into +0.0).
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
@@ -911,7 +923,7 @@ __device__ bool adj_refine(const TT* row, int V, bool vec, float M, float c, flo
       const uint32_t s = (hi - k) / w;
       if (s >= (uint32_t)kAdjBins2) return;  // cannot happen; guard only
       atomicAdd(&A.cnt2[s], 1u);
-      atomicAdd(&A.mass2[s], __float2ull_rn(pow2_neg((M - x) * c) * fscale));
+      atomicAdd(&A.mass2[s], adj_mass((M - x) * c, fscale));
       atomicMin(&A.kmin2[s], k);
       atomicMax(&A.kmax2[s], k);
     });
@@ -956,12 +968,12 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
     const float z = (M - x) * c;
     const int b = adj_bin1(z, g);
     if (b < 0) {
-      if (far_mass) fm += __float2ull_rn(pow2_neg(z) * fscale);
+      if (far_mass) fm += adj_mass(z, fscale);
       return;
     }
     const uint32_t k = order_key(x);
     atomicAdd(&A.cnt1[b], 1u);
-    atomicAdd(&A.mass1[b], __float2ull_rn(pow2_neg(z) * fscale));
+    atomicAdd(&A.mass1[b], adj_mass(z, fscale));
     atomicMin(&A.kmin1[b], k);
     atomicMax(&A.kmax1[b], k);
   });
@@ -1056,9 +1068,8 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
                            float top_p, bool use_k, bool use_p, uint64_t pol, AdjShared& A,
                            float& tau, float& S, unsigned long long* ctr) {
   // masses are pow2_neg(z) * 2^F with V * 2^F <= 2^62
-  const int lg = V > 1 ? 32 - __clz(V - 1) : 0;
-  const int F = 62 - lg;
-  const float fscale = __int_as_float((127 + F) << 23);
+  const int F = adj_mass_shift(V);
+  const float fscale = adj_mass_scale(F);
   const double unscale = __longlong_as_double((long long)(1023 - F) << 52);
   uint32_t key = 0u;
   unsigned long long kept = 0ull;
@@ -2443,6 +2454,19 @@ static __global__ void neglog_fill_kernel(uint32_t k0, int64_t n, float* out) {
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
        j += (int64_t)gridDim.x * blockDim.x)
     out[j] = neg_log_uniform(k0 + (uint32_t)j);
+}
+
+// The selection's integer mass and 2^-z of entries at distances z from the
+// row maximum, for a row of V entries: used by the tests of the mass definition.
+static __global__ void selection_mass_kernel(const float* z, int64_t n, int V,
+                                             unsigned long long* mass, float* p2) {
+  const float fscale = adj_mass_scale(adj_mass_shift(V));
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+       j += (int64_t)gridDim.x * blockDim.x) {
+    const float zj = z[j];
+    if (mass) mass[j] = adj_mass(zj, fscale);
+    if (p2) p2[j] = pow2_neg(zj);
+  }
 }
 
 }  // namespace specdec

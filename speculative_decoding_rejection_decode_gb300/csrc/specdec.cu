@@ -527,6 +527,17 @@ int specdec_neg_log_uniform(uint32_t k0, int64_t n, float* out, void* stream) {
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
+int specdec_selection_mass(const float* z, int64_t n, int V, uint64_t* out_mass, float* out_pow2,
+                           void* stream) {
+  if (n < 0 || V <= 0 || V > (1 << 30) || (n > 0 && (!z || (!out_mass && !out_pow2))))
+    return SPECDEC_ERR_INVALID_ARG;
+  if (n == 0) return SPECDEC_OK;
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  selection_mass_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      z, n, V, reinterpret_cast<unsigned long long*>(out_mass), out_pow2);
+  return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
 const char* specdec_status_string(int status) {
   switch (status) {
     case SPECDEC_OK: return "ok";

@@ -11,6 +11,7 @@ from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_DU
                    SPECDEC_PATH_FUSED, SPECDEC_PATH_GREEDY, SPECDEC_PATH_PAIR, SPECDEC_PATH_STREAM, SPECDEC_PATH_SWEEP,
                    SPECDEC_PATH_TWO_PASS, specdec_create, specdec_destroy,
                    specdec_get_error, specdec_last_path, specdec_neg_log_uniform,
+                   specdec_selection_mass,
                    specdec_rejection_sample, specdec_rejection_sample_ex,
                    specdec_rejection_sample_noalloc, specdec_rejection_sample_topk_topp,
                    specdec_reserve, specdec_set_adjust_counters,
@@ -180,6 +181,19 @@ def uniform(seed: int, b: int, pos: int, stream_id: int, v0: int, n: int,
     _check(specdec_uniform(seed, b, pos, stream_id, v0, n, out.data_ptr(), _stream_handle(dev)),
            "specdec_uniform")
     return out
+
+
+def selection_mass(z: torch.Tensor, V: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """The top-p selection's integer masses (int64 holding the uint64 values,
+    all below 2^63) and 2^-z (float32) for float32 distances z on the device."""
+    if z.dtype != torch.float32 or not z.is_cuda:
+        raise ValueError("z must be a float32 CUDA tensor")
+    z = z.contiguous()
+    mass = torch.empty(z.numel(), dtype=torch.int64, device=z.device)
+    p2 = torch.empty(z.numel(), dtype=torch.float32, device=z.device)
+    _check(specdec_selection_mass(z.data_ptr(), z.numel(), V, mass.data_ptr(), p2.data_ptr(),
+                                  _stream_handle(z.device)), "specdec_selection_mass")
+    return mass, p2
 
 
 def neg_log_uniform(k0: int, n: int, device: int | torch.device = 0) -> torch.Tensor:

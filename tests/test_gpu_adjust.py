@@ -34,6 +34,34 @@ def _check(V, w, tk, tp, budget=True):
     return g, r
 
 
+@pytest.mark.parametrize("vocab", [1, 2, 3, 1000, 32000, 151936, 256000, 262145, 1 << 30])
+def test_selection_mass_bit_exact(V, vocab):
+    # the top-p masses (2^-z and its integer scaling) on the device equal the
+    # oracle's independent implementation of the same written definition
+    import oracle
+    from speculative_decoding_rejection_decode_gb300 import selection_mass
+    rng = np.random.default_rng(vocab % 1000)
+    ints = np.arange(0, 70, dtype=np.float32)
+    z = np.concatenate([
+        rng.uniform(0, 70, 200000), rng.uniform(0, 1, 50000), rng.uniform(40, 64, 50000),
+        ints, np.nextafter(ints, np.float32(np.inf)), np.nextafter(ints, np.float32(-np.inf))[1:],
+        [-0.0, 63.99999, 64.0, 1e30, np.inf, np.nan]]).astype(np.float32)
+    want_m, want_p = oracle.selection_mass(z, vocab)
+    got_m, got_p = selection_mass(torch.from_numpy(z).cuda(), vocab)
+    got_m = got_m.cpu().numpy().view(np.uint64)
+    got_p = got_p.cpu().numpy()
+    assert np.array_equal(got_p.view(np.uint32), want_p.view(np.uint32))
+    assert np.array_equal(got_m, want_m)
+
+
+def test_selection_mass_argument_checks(V):
+    from speculative_decoding_rejection_decode_gb300 import specdec_selection_mass
+    assert specdec_selection_mass(None, -1, 10, None, None, None) != 0
+    assert specdec_selection_mass(None, 4, 10, None, None, None) != 0
+    assert specdec_selection_mass(None, 0, 0, None, None, None) != 0
+    assert specdec_selection_mass(None, 0, 10, None, None, None) == 0
+
+
 @pytest.mark.parametrize("idx", [0, 1, 3])
 def test_standard_workloads_with_mixed_settings(V, idx):
     w = make_config(idx, device="cuda")

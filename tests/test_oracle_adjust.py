@@ -51,6 +51,27 @@ def test_pow2_neg_definition():
     assert np.all(np.diff(g) <= 0)
 
 
+def test_selection_mass_definition():
+    # the integer mass 2^-z * 2^F rounded to the nearest integer, ties to even,
+    # with F = 62 - ceil(log2 V): F from V's powers of two, exact powers of two
+    # at integer z, 1/2 rounds to 0 and 2^-1/2 to 1, nothing past z = 64, a row
+    # of V entries at the maximum sums to at most 2^62, and 2^-z as above
+    for V, F in [(1, 62), (2, 61), (3, 60), (4, 60), (5, 59), (32000, 47), (151936, 44),
+                 (256000, 44), (262144, 44), (262145, 43), (1 << 30, 32)]:
+        z = np.array([0.0, 1.0, 5.0, F - 1.0, float(F), F + 0.5, F + 1.0, F + 2.0, 64.0],
+                     np.float32)
+        mass, p2 = oracle.selection_mass(z, V)
+        assert mass.dtype == np.uint64
+        assert [int(m) for m in mass] == [2 ** F, 2 ** (F - 1), 2 ** (F - 5), 2, 1, 1, 0, 0, 0], V
+        assert V * int(mass[0]) <= 2 ** 62
+        assert np.array_equal(p2, np.array([oracle.pow2_neg(float(x)) for x in z], np.float32))
+    mass, _ = oracle.selection_mass(np.array([np.nan, np.inf, 1e30], np.float32), 1000)
+    assert mass.tolist() == [0, 0, 0]
+    # non-increasing in z
+    m, _ = oracle.selection_mass(np.linspace(0, 50, 20001, dtype=np.float32), 256000)
+    assert np.all(np.diff(m.astype(np.float64)) <= 0)
+
+
 def test_closed_forms():
     # p = (1/2, 1/4, 1/8, 1/8) at T = 1
     l = _f32(np.log([4.0, 2.0, 1.0, 1.0]))
