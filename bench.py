@@ -460,7 +460,9 @@ def main():
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes_rows,
                      "avg_launch_ms": row_avg_ms, "min_launch_ms": min(row_ms),
+                     "median_launch_ms": statistics.median(row_ms),
                      "share_of_step": row_avg_ms / statistics.mean(step_ms)},
+        "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
         "path": path_name, "cluster_size": csize,
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
