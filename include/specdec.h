@@ -42,11 +42,13 @@
  * Ownership: the caller owns every input and output buffer (device memory).  The
  * handle owns a device workspace (per-row softmax statistics, adjusted-row
  * thresholds, status words, greedy keys and the dual kernel's halves, 80 bytes
- * per target row, plus 1036
- * bytes per request) and
- * one stream-ordered error word.  A handle serves one stream at a time; calls on it are
- * asynchronous and never synchronise, except the first call that needs a larger
- * workspace than specdec_reserve() provided (it reads cu[B] back to size it).
+ * per target row, plus 1036 bytes per request) and one stream-ordered error
+ * word.  A handle serves one stream at a time; calls on it are asynchronous and
+ * never synchronise, except the first call that needs a larger workspace than
+ * specdec_reserve() provided (it reads cu[B] back to size it).  A call on a
+ * handle makes the handle's device current while it runs and restores the
+ * calling thread's current device before it returns; the stream must belong to
+ * the handle's device.  Calls without a handle run on the current device.
  *
  * Errors: host-checked problems return a negative status before anything is
  * launched.  Problems only the device can see (a draft id outside [0, V), a

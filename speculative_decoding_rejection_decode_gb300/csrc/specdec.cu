@@ -70,6 +70,32 @@ namespace {
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Makes the handle's device current for one entry-point call and puts the
+// caller's current device back when the call returns, so that no call changes
+// which device the calling thread works on.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int device) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      prev_ = -1;
+    }
+    ok_ = prev_ == device || cudaSetDevice(device) == cudaSuccess;
+    restore_ = ok_ && prev_ >= 0 && prev_ != device;
+  }
+  ~DeviceGuard() {
+    if (restore_) cudaSetDevice(prev_);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = false;
+  bool restore_ = false;
+};
+
 int free_workspace(specdec_ctx* h) {
   if (h->ws.base) {
     cudaFree(h->ws.base);
@@ -101,7 +127,10 @@ int alloc_workspace(specdec_ctx* h, int64_t rows, int b) {
     cudaGetLastError();
     return SPECDEC_ERR_OOM;
   }
-  if (cudaMemset(p, 0, total) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (cudaMemset(p, 0, total) != cudaSuccess) {
+    cudaFree(p);
+    return SPECDEC_ERR_CUDA;
+  }
   char* c = static_cast<char*>(p);
   h->ws.base = p;
   h->ws.row_stats = reinterpret_cast<float2*>(c);
@@ -319,7 +348,8 @@ int specdec_create(specdec_handle_t* out, int device) {
     return SPECDEC_ERR_CUDA;
   }
   if (device < 0 || device >= n) return SPECDEC_ERR_INVALID_ARG;
-  if (cudaSetDevice(device) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  DeviceGuard guard(device);
+  if (!guard.ok()) return SPECDEC_ERR_CUDA;
   specdec_ctx* h = new (std::nothrow) specdec_ctx();
   if (!h) return SPECDEC_ERR_OOM;
   h->device = device;
@@ -335,9 +365,15 @@ int specdec_create(specdec_handle_t* out, int device) {
     const int v = std::atoi(e);
     if (v == 1 || v == 2) h->stream_ctas = v;
   }
-  if (cudaMalloc(&h->small, 64) != cudaSuccess || cudaMemset(h->small, 0, 64) != cudaSuccess) {
+  if (cudaMalloc(&h->small, 64) != cudaSuccess) {
+    cudaGetLastError();
     delete h;
     return SPECDEC_ERR_OOM;
+  }
+  if (cudaMemset(h->small, 0, 64) != cudaSuccess) {
+    cudaFree(h->small);
+    delete h;
+    return SPECDEC_ERR_CUDA;
   }
   *out = h;
   return SPECDEC_OK;
@@ -345,7 +381,8 @@ int specdec_create(specdec_handle_t* out, int device) {
 
 int specdec_reserve(specdec_handle_t h, int64_t max_draft_positions, int max_batch) {
   if (!h || max_draft_positions < 0 || max_batch <= 0) return SPECDEC_ERR_INVALID_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return SPECDEC_ERR_CUDA;
   h->reserved = true;
   h->res_rows = max_draft_positions + max_batch;
   h->res_b = max_batch;
@@ -365,7 +402,8 @@ int specdec_rejection_sample_topk_topp(
   if (!std::isfinite(T) || T < 0.0f) return SPECDEC_ERR_INVALID_ARG;
   if (!target_logits || !draft_ids || !cu_num_draft_tokens || !out_tokens || !out_num_accepted)
     return SPECDEC_ERR_INVALID_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return SPECDEC_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = ensure_capacity(h, cu_num_draft_tokens, B, st);
   if (rc != SPECDEC_OK) return rc;
@@ -471,7 +509,8 @@ int specdec_rejection_sample(specdec_handle_t h, const void* target_logits, int 
 
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream) {
   if (!h || !device_error) return SPECDEC_ERR_INVALID_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return SPECDEC_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, h->small, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -554,7 +593,7 @@ const char* specdec_status_string(int status) {
 
 int specdec_destroy(specdec_handle_t h) {
   if (!h) return SPECDEC_ERR_INVALID_ARG;
-  cudaSetDevice(h->device);
+  DeviceGuard guard(h->device);
   cudaDeviceSynchronize();
   free_workspace(h);
   if (h->small) cudaFree(h->small);
