@@ -66,7 +66,7 @@ class Workload:
                         mv(self.cu), dict(self.meta))
 
 
-CONFIGS = {
+STANDARD_WORKLOADS = {
     0: dict(name="tiny B=1 gamma=4 V=32 f32 T=1", B=1, gamma=4, V=32, dtype="f32", T=1.0,
             target_std=2.0, noise_std=0.5, draft_T=1.0, ids="sample"),
     1: dict(name="B=8 gamma=5 V=32000 f32 T=1", B=8, gamma=5, V=32000, dtype="f32", T=1.0,
@@ -82,8 +82,8 @@ CONFIGS = {
 
 def make_config(idx: int, device="cpu", B: int | None = None, V: int | None = None,
                 chunk_rows: int = 512) -> Workload:
-    """Workload ``idx`` (0..4), optionally with a smaller batch or vocabulary."""
-    c = dict(CONFIGS[idx])
+    """Standard workload ``idx`` (0..4), optionally with a smaller batch or vocabulary."""
+    c = dict(STANDARD_WORKLOADS[idx])
     if B is not None:
         c["B"] = B
     if V is not None:
