@@ -1,6 +1,7 @@
 """Host logic of bench.py on CPU: the all-cores oracle rate covers every request
 once, the clock sampler's parsing and throttle flags, the committed DRAM-traffic
-record's validity checks and the top-k / top-p settings of the adjusted lines."""
+record's validity checks, the top-k / top-p settings of the adjusted lines, and
+the reference arm under a two-rank torchrun launch (gloo)."""
 import argparse
 import os
 
@@ -97,3 +98,32 @@ def test_adjust_settings():
     tk2, tp2 = bench.adjust_settings(w, _args(adjust_mix=True), "cpu")
     assert torch.equal(tk1, tk2) and torch.equal(tp1, tp2)     # seeded
     assert bench.adjust_desc(_args(adjust_mix=True)) == "seeded per-request mix"
+
+
+def test_reference_arm_two_ranks_rank0_prints_once():
+    # the launch the driver uses for N > 1 (torchrun, one process per rank, gloo
+    # here): rank 0 alone times the oracle and prints one line, the other rank
+    # exits 0 without work
+    import json
+    import socket
+    import subprocess
+    import sys
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+           "reference", "--gpus", "2", "--config", "1", "--steps", "2", "--warmup", "1"]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["metric"] == "verified draft positions/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
