@@ -38,6 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["speculative_decoding_rejection_decode_gb300/csrc/kernels.cuh",
                   "speculative_decoding_rejection_decode_gb300/csrc/device_common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "row_kernel_traffic_large_workload.txt")
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e data-sheet bandwidth (context beside the measured peak)
 
 
 def parse_args():
@@ -458,6 +459,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": kernel_name,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": alg_bytes_rows,
                      "avg_launch_ms": row_avg_ms, "min_launch_ms": min(row_ms),
                      "median_launch_ms": statistics.median(row_ms),
