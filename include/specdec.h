@@ -103,8 +103,8 @@ typedef struct specdec_ctx* specdec_handle_t;
                                    the second to finish combines (T > 0)            */
 
 /* Creates a handle bound to CUDA device `device`.  *out receives the handle.
- * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (null out, bad device) or
- * SPECDEC_ERR_CUDA. */
+ * Returns SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (null out, bad device),
+ * SPECDEC_ERR_OOM or SPECDEC_ERR_CUDA. */
 int specdec_create(specdec_handle_t* out, int device);
 
 /* Pre-sizes the workspace for calls with cu[B] <= max_draft_positions and
@@ -114,8 +114,9 @@ int specdec_create(specdec_handle_t* out, int device);
 int specdec_reserve(specdec_handle_t h, int64_t max_draft_positions, int max_batch);
 
 /* One verify step for B requests (see the top of this file for the layout).
- *   target_logits      device [N_t, V] of `dtype`; 16-byte aligned rows take the
- *                      single-pass path, other strides a two-pass path
+ *   target_logits      device [N_t, V] of `dtype`; any alignment (16-byte aligned
+ *                      rows, with draft rows to match, are read with 16-byte
+ *                      vector loads, other rows element by element)
  *   dtype              SPECDEC_F32 or SPECDEC_BF16
  *   draft_probs        device [N_d, V] float32 rows of q (taken as given, not
  *                      renormalised); ignored when T == 0.  NULL at T > 0 means
@@ -190,8 +191,8 @@ int specdec_rejection_sample_topk_topp(
 
 /* Reads the handle's sticky device error word (SPECDEC_DEVERR_* bits) into
  * *device_error and clears it.  Queues the read on `stream` and waits for it, so
- * it reports every call queued on that stream before it.  Returns SPECDEC_OK or
- * SPECDEC_ERR_CUDA. */
+ * it reports every call queued on that stream before it.  Returns SPECDEC_OK,
+ * SPECDEC_ERR_INVALID_ARG (null handle or pointer) or SPECDEC_ERR_CUDA. */
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream);
 
 /* Forces an execution path for T > 0 (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
