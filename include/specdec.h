@@ -219,7 +219,8 @@ int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after
 int specdec_set_adjust_counters(specdec_handle_t h, uint64_t* device_counters);
 
 /* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
- * _STREAM, _PAIR or _GREEDY), and the cluster size of a cluster path (0 otherwise). */
+ * _STREAM, _PAIR, _DUAL or _GREEDY), and the cluster size of a cluster path (0
+ * otherwise). */
 int specdec_last_path(specdec_handle_t h, int* path, int* cluster_size);
 
 /* Writes out[j] = U(seed, b, pos, stream_id, v0 + j) for j < n into device
@@ -249,7 +250,7 @@ int specdec_selection_mass(const float* z, int64_t n, int V, uint64_t* out_mass,
                            void* stream);
 
 /* ---- allocation-free variant -----------------------------------------------
- * No counterpart in the paper: this entry point exists for callers that cannot
+ * No counterpart in the pages: this entry point exists for callers that cannot
  * allocate device memory at the point where they verify (code running inside a
  * memory pool or arena it does not own, plug-ins that are handed only
  * pre-allocated buffers, hosts that freeze device allocation after start-up).
