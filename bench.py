@@ -41,7 +41,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "row_kernel_traffic_large_workload
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e data-sheet bandwidth (context beside the measured peak)
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -66,7 +66,20 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--secondary", type=int, default=None,
+                    help="a second standard workload timed in the same run and reported as "
+                         "'secondary' (default: the ragged workload 3 beside the plain large "
+                         "workload 4; -1: none)")
+    ap.add_argument("--secondary-steps", type=int, default=200)
+    args = ap.parse_args(argv)
+    if args.secondary is None:
+        plain = (args.config == 4 and args.batch is None and args.vocab is None
+                 and args.draft == "probs" and args.path == "auto" and args.top_k is None
+                 and args.top_p is None and not args.adjust_mix)
+        args.secondary = 3 if plain else -1
+    if args.secondary < 0:
+        args.secondary = None
+    return args
 
 
 # ----------------------------------------------------------------------------
@@ -176,9 +189,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_key: str, kernel: str):
-    """DRAM bytes per launch of the row kernel from the committed ncu summary,
-    when it was taken on the current kernel source and this workload."""
+def recorded_traffic(workload_key: str, kernel: str, alg_bytes: int):
+    """DRAM bytes per launch of the row kernel, scaled from the committed ncu
+    summary: that record holds the DRAM bytes per algorithmic byte of one
+    launch captured on a smaller batch of the same workload (same vocabulary,
+    dtypes and draft depth; the batch is left out of the key), taken on the
+    current kernel source.  None when no such record exists."""
     try:
         vals = {}
         for line in open(TRAFFIC_FILE):
@@ -189,7 +205,7 @@ def recorded_traffic(workload_key: str, kernel: str):
             return None
         if vals.get("workload_key") != workload_key or vals.get("kernel") != kernel:
             return None
-        return float(vals["traffic_bytes_per_launch"])
+        return float(vals["traffic_bytes_per_algorithmic_byte"]) * alg_bytes
     except (OSError, KeyError, ValueError):
         return None
 
@@ -237,7 +253,7 @@ def oracle_threaded_rate(w, seconds: float, threads: int, top_k=None, top_p=None
     from speculative_decoding_rejection_decode_gb300.inputs import to_numpy_logits
     from speculative_decoding_rejection_decode_gb300.sharding import shard_bounds
     oracle.build()
-    oracle.pow2_neg(1.0)          # loads the library once, before the threads start
+    oracle.splitmix64(0)          # loads the library once, before the threads start
     cu = w.cu.cpu().numpy().astype("int64")
     tk = None if top_k is None else top_k.cpu().numpy()
     tp = None if top_p is None else top_p.cpu().numpy()
@@ -291,14 +307,15 @@ def host_cpu_model() -> str:
     return platform.machine()
 
 
-def adjust_settings(w, args, device):
+def adjust_settings(w, args, device, config=None):
     """Per-request top-k / top-p tensors for the adjusted-target bench lines
     (None, None for the plain verify step)."""
     if args.top_k is None and args.top_p is None and not args.adjust_mix:
         return None, None
     from speculative_decoding_rejection_decode_gb300.inputs import make_top_k_top_p
     if args.adjust_mix:
-        return make_top_k_top_p(w.B, w.V, seed=1000 + args.config, device=device)
+        cfg = args.config if config is None else config
+        return make_top_k_top_p(w.B, w.V, seed=1000 + cfg, device=device)
     return make_top_k_top_p(w.B, w.V, seed=0, top_k=args.top_k, top_p=args.top_p, device=device)
 
 
@@ -310,10 +327,10 @@ def adjust_desc(args):
     return {"top_k": args.top_k, "top_p": args.top_p}
 
 
-def workload_desc(w, args, flush: bool, in_bytes: int) -> dict:
+def workload_desc(w, args, flush: bool, in_bytes: int, config=None) -> dict:
     gam = w.meta.get("gamma")
     d = {
-        "workload": f"{w.name} (standard workload {args.config})",
+        "workload": f"{w.name} (standard workload {args.config if config is None else config})",
         "B": w.B, "gamma": list(gam) if isinstance(gam, tuple) else gam, "V": w.V,
         "target_dtype": w.dtype, "draft_dtype": None if w.draft_probs is None else "f32",
         "T": w.T, "n_draft_positions": w.n_draft, "n_target_rows": w.n_target,
@@ -327,24 +344,21 @@ def workload_desc(w, args, flush: bool, in_bytes: int) -> dict:
     return d
 
 
-def main():
-    args = parse_args()
-    dist = Dist()
+class Measured:
+    """One workload timed on the GPU: the JSON fields and what the extra legs
+    (selection counters, acceptance, e2e, CPU baseline) need."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def measure(args, dist, dev, sd, config: int, steps: int, warmup: int) -> Measured:
+    """Times `steps` verify steps of standard workload `config` (after `warmup`
+    untimed ones) with CUDA events on the call's stream, the row kernel timed
+    by events the library records around it."""
     import torch
     from speculative_decoding_rejection_decode_gb300.inputs import make_config
-
-    if args.impl == "reference":
-        run_reference(args, dist)
-        dist.close()
-        return
-
-    from speculative_decoding_rejection_decode_gb300.build import build
-    build()
-    import speculative_decoding_rejection_decode_gb300 as sd
-
-    dev = torch.device("cuda", dist.local_rank)
-    torch.cuda.set_device(dev)
-    w = make_config(args.config, device=dev, B=args.batch, V=args.vocab)
+    w = make_config(config, device=dev, B=args.batch, V=args.vocab)
     if args.draft == "onehot":
         w.draft_probs = None
         w.name += " one-hot drafts"
@@ -355,8 +369,8 @@ def main():
     flush = in_bytes < 4 * L2_BYTES
     alg_bytes_step = w.algorithmic_bytes()       # + one extra target row per request
     alg_bytes_rows = tgt_bytes + drf_bytes       # what the row kernel must read
-    workload_key = f"config{args.config}-B{w.B}-V{w.V}-{args.path}"
-    tk, tp = adjust_settings(w, args, dev)
+    workload_key = f"config{config}-V{w.V}-{w.dtype}-{args.draft}"
+    tk, tp = adjust_settings(w, args, dev, config)
     if tk is not None:
         workload_key += "-adjusted"
 
@@ -384,7 +398,7 @@ def main():
         v(w.target_logits, w.draft_probs, w.draft_ids, w.cu, w.T, w.seed, out=out,
           request_offset=offset, top_k=tk, top_p=tp)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         if flush:
             flush_l2()
         step()
@@ -404,7 +418,7 @@ def main():
     path_name = {1: "fused", 2: "two_pass", 3: "sweep", 4: "greedy", 5: "stream", 6: "pair",
                  7: "dual"}[path]
 
-    K = args.steps
+    K = steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
@@ -445,13 +459,13 @@ def main():
     row_avg_ms = statistics.mean(row_ms)
     peak, peak_kind = measured_peak_gbs()
     achieved = alg_bytes_rows / (row_avg_ms / 1e3) / 1e9
-    traffic = recorded_traffic(workload_key, kernel_name)
+    traffic = recorded_traffic(workload_key, kernel_name, alg_bytes_rows)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": max(3, warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_desc(w, args, flush, in_bytes),
+        "config": workload_desc(w, args, flush, in_bytes, config),
         "requests_per_s": w.B * dist.world * K / total_s,
         "achieved_gbps_step": alg_bytes_step / (ms_per_step / 1e3) / 1e9,
         "algorithmic_bytes_per_step": alg_bytes_step,
@@ -470,6 +484,45 @@ def main():
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
+    return Measured(result=result, v=v, w=w, out=out, stream=stream, offset=offset, tk=tk, tp=tp,
+                    step=step)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    import torch
+
+    if args.impl == "reference":
+        run_reference(args, dist)
+        dist.close()
+        return
+
+    from speculative_decoding_rejection_decode_gb300.build import build
+    build()
+    import speculative_decoding_rejection_decode_gb300 as sd
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    # the second workload the roofline target names (the ragged batch), timed in
+    # the same run and reported beside the headline as "secondary"
+    secondary = None
+    if args.secondary is not None and args.secondary != args.config:
+        m2 = measure(args, dist, dev, sd, args.secondary, args.secondary_steps, args.warmup)
+        r2 = m2.result
+        secondary = {k: r2[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",
+                                        "requests_per_s", "achieved_gbps_step",
+                                        "algorithmic_bytes_per_step", "frac_step_of_peak",
+                                        "roofline", "step_ms_median", "step_ms_min", "path",
+                                        "cluster_size", "gpu_launches", "clocks")}
+        m2.v.close()
+        del m2
+        torch.cuda.empty_cache()
+    m = measure(args, dist, dev, sd, args.config, args.steps, args.warmup)
+    result, v, w, out, stream = m.result, m.v, m.w, m.out, m.stream
+    offset, tk, tp, step = m.offset, m.tk, m.tp, m.step
+    if secondary is not None:
+        result["secondary"] = secondary
 
     if tk is not None:
         # one more step with the selection counters on (outside the timed region)

@@ -264,13 +264,20 @@ int specdec_selection_mass(const float* z, int64_t n, int V, uint64_t* out_mass,
  *   out_device_error   optional device word; SPECDEC_DEVERR_* bits are OR-ed
  *                      into it (the caller clears it); NULL drops them
  * Limits: cu[B] + B <= SPECDEC_NOALLOC_MAX_ROWS and B <= SPECDEC_NOALLOC_MAX_BATCH;
- * larger calls return SPECDEC_ERR_CAPACITY before anything is queued.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and caches it: make that first call before any stream
- * capture.  Every call on a device shares the one array and it keeps the last
- * call's contents; each call clears the counters it needs at its start, on its
- * stream.  Calls whose work overlaps on the GPU (two streams, two host threads)
- * race on the array and must be serialised by the caller. */
+ * larger calls return SPECDEC_ERR_CAPACITY before anything is queued.  The
+ * check trusts n_draft_positions: when it is below the device's cu[B] and the
+ * real rows pass the limit, the kernels skip the rows past it and set
+ * SPECDEC_DEVERR_CAPACITY, and the outputs of the requests that own them are
+ * left unwritten -- with out_device_error NULL the call then reports nothing.
+ * Every call made outside stream capture looks up the array's device address
+ * (cudaGetSymbolAddress, a host-side query; after cudaDeviceReset the array
+ * may sit elsewhere); a call made while `stream` is capturing reuses the
+ * address of the last call on that device outside capture, so make the first
+ * call on a device before any capture.  Every call on a device shares the one
+ * array and it keeps the last call's contents; each call clears what it
+ * accumulates into at its start, on its stream.  Calls whose work overlaps on
+ * the GPU (two streams, two host threads) race on the array and must be
+ * serialised by the caller. */
 #define SPECDEC_NOALLOC_MAX_ROWS 16384
 #define SPECDEC_NOALLOC_MAX_BATCH 4096
 int specdec_rejection_sample_noalloc(const void* target_logits, int dtype,

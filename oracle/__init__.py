@@ -79,16 +79,13 @@ def _load():
                                                 vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_rejection_sample.restype = i32
         lib.oracle_verify_request_adj.argtypes = [i64, i32, vp, i32, vp, vp, i32, dbl, i32, dbl,
-                                                  u64, vp, vp, vp, vp, vp, vp, vp, vp]
+                                                  vp, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                  vp]
         lib.oracle_verify_request_adj.restype = i32
         lib.oracle_rejection_sample_adj.argtypes = [vp, i32, vp, vp, vp, i32, i32, dbl, vp, vp,
-                                                    u64, vp, vp, vp, vp, vp, vp, vp, vp]
-        lib.oracle_pow2_neg.argtypes = [ctypes.c_float]
-        lib.oracle_pow2_neg.restype = ctypes.c_float
-        lib.oracle_selection_mass.argtypes = [vp, i64, i32, vp, vp]
-        lib.oracle_selection_mass.restype = None
+                                                    u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_rejection_sample_adj.restype = i32
-        lib.oracle_adjusted_probs.argtypes = [vp, i32, i32, dbl, i32, dbl, vp]
+        lib.oracle_adjusted_probs.argtypes = [vp, i32, i32, dbl, i32, dbl, i32, vp, vp, vp]
         lib.oracle_adjusted_probs.restype = i32
         _lib = lib
         return lib
@@ -141,6 +138,8 @@ class OracleResult:
     pos_near_tie: np.ndarray    # int32 [N_d]
     near_tie: np.ndarray        # int32 [B]
     status: int
+    edge_lo: np.ndarray | None = None   # int32 [N_t]  reachable top-p cut shifts of each
+    edge_hi: np.ndarray | None = None   # int32 [N_t]  target row (0 / 0 without a band)
 
 
 def _per_request(a, B: int, dtype, name: str):
@@ -182,19 +181,25 @@ def rejection_sample(target_logits: np.ndarray, draft_probs: np.ndarray | None,
     acc = np.empty(max(n_d, 1), np.int32)
     pos_tie = np.empty(max(n_d, 1), np.int32)
     tie = np.empty(B, np.int32)
+    elo = np.zeros(n_t, np.int32)
+    ehi = np.zeros(n_t, np.int32)
     st = lib.oracle_rejection_sample_adj(_ptr(logits), dt, _ptr(q), _ptr(ids), _ptr(cu), B, V,
                                          float(T), _ptr(tk), _ptr(tp), seed & 0xFFFFFFFFFFFFFFFF,
                                          _ptr(tokens), _ptr(nacc), _ptr(beta), _ptr(p_x), _ptr(q_x),
-                                         _ptr(acc), _ptr(pos_tie), _ptr(tie))
+                                         _ptr(acc), _ptr(pos_tie), _ptr(tie), _ptr(elo), _ptr(ehi))
     return OracleResult(tokens, nacc, beta[:n_d], p_x[:n_d], q_x[:n_d], acc[:n_d], pos_tie[:n_d],
-                        tie, int(st))
+                        tie, int(st), elo, ehi)
 
 
 def verify_request(b: int, target_rows: np.ndarray, draft_rows: np.ndarray | None,
                    draft_ids: np.ndarray, T: float, seed: int,
-                   dtype: str | None = None, top_k: int = 0, top_p: float = 1.0) -> OracleResult:
+                   dtype: str | None = None, top_k: int = 0, top_p: float = 1.0,
+                   edge_shift=None) -> OracleResult:
     """One request with global request index ``b`` (the generator key), its
-    gamma+1 target rows and gamma draft rows."""
+    gamma+1 target rows and gamma draft rows.  ``edge_shift`` (gamma+1 ints or
+    None) moves each row's top-p cut by that many groups within the row's
+    reachable range (``edge_lo`` / ``edge_hi`` of the result); a shift outside
+    it gives status INVALID_ARG."""
     lib = _load()
     logits, dt = _logits_array(target_rows, dtype)
     V = logits.shape[-1]
@@ -203,45 +208,40 @@ def verify_request(b: int, target_rows: np.ndarray, draft_rows: np.ndarray | Non
     if ids.shape[0] != gamma:
         raise ValueError("need gamma draft ids for gamma+1 target rows")
     q = None if draft_rows is None else np.ascontiguousarray(draft_rows, dtype=np.float32)
+    shift = None
+    if edge_shift is not None:
+        shift = np.ascontiguousarray(edge_shift, dtype=np.int32)
+        if shift.shape != (gamma + 1,):
+            raise ValueError("edge_shift needs one value per target row")
     g1 = max(gamma, 1)
     tokens = np.empty(gamma + 1, np.int32)
     nacc = np.empty(1, np.int32)
     beta, p_x, q_x = (np.empty(g1, np.float64) for _ in range(3))
     acc, pos_tie = np.empty(g1, np.int32), np.empty(g1, np.int32)
     tie = np.empty(1, np.int32)
+    elo = np.zeros(gamma + 1, np.int32)
+    ehi = np.zeros(gamma + 1, np.int32)
     st = lib.oracle_verify_request_adj(b, gamma, _ptr(logits), dt, _ptr(q), _ptr(ids), V, float(T),
-                                       int(top_k), float(top_p), seed & 0xFFFFFFFFFFFFFFFF,
-                                       _ptr(tokens), _ptr(nacc), _ptr(beta), _ptr(p_x), _ptr(q_x),
-                                       _ptr(acc), _ptr(pos_tie), _ptr(tie))
+                                       int(top_k), float(top_p), _ptr(shift),
+                                       seed & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(nacc),
+                                       _ptr(beta), _ptr(p_x), _ptr(q_x), _ptr(acc), _ptr(pos_tie),
+                                       _ptr(tie), _ptr(elo), _ptr(ehi))
     return OracleResult(tokens, nacc, beta[:gamma], p_x[:gamma], q_x[:gamma], acc[:gamma],
-                        pos_tie[:gamma], tie, int(st))
-
-
-def pow2_neg(z: float) -> float:
-    """2^-z on the float32 definition the top-p edge is decided with."""
-    return float(_load().oracle_pow2_neg(float(z)))
-
-
-def selection_mass(z: np.ndarray, V: int) -> tuple[np.ndarray, np.ndarray]:
-    """Integer masses (uint64) and 2^-z (float32) of entries at float32
-    distances z from the maximum of a row of V entries, on the definition the
-    top-p edge is decided with."""
-    z = np.ascontiguousarray(z, dtype=np.float32)
-    mass = np.empty(z.shape[0], np.uint64)
-    p2 = np.empty(z.shape[0], np.float32)
-    _load().oracle_selection_mass(_ptr(z), z.shape[0], int(V), _ptr(mass), _ptr(p2))
-    return mass, p2
+                        pos_tie[:gamma], tie, int(st), elo, ehi)
 
 
 def adjusted_probs(row: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0,
-                   dtype: str | None = None) -> np.ndarray:
+                   dtype: str | None = None, shift: int = 0, with_range: bool = False):
     """The adjusted target distribution of one row of logits (temperature,
-    then top-k, then top-p)."""
+    then top-k, then top-p), with the top-p cut moved by ``shift`` groups.
+    With ``with_range`` also the reachable range (lo, hi) of shifts."""
     lib = _load()
     logits, dt = _logits_array(np.asarray(row).reshape(-1), dtype)
     p = np.empty(logits.shape[0], np.float64)
+    lo = np.zeros(1, np.int32)
+    hi = np.zeros(1, np.int32)
     st = lib.oracle_adjusted_probs(_ptr(logits), dt, logits.shape[0], float(T), int(top_k),
-                                   float(top_p), _ptr(p))
+                                   float(top_p), int(shift), _ptr(p), _ptr(lo), _ptr(hi))
     if st < 0:
         raise ValueError(f"oracle_adjusted_probs failed with status {st}")
-    return p
+    return (p, (int(lo[0]), int(hi[0]))) if with_range else p

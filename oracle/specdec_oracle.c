@@ -58,10 +58,14 @@
  *         smallest top set whose mass reaches P, ties at its edge included);
  *       p'(v) = e(v) / (sum of e over the kept tokens) on the kept tokens, 0
  *         elsewhere.  Draft probabilities are taken as already adjusted.
- *     T == 0 ignores both (the argmax is always kept).  The top-p edge is a
- *     decision that floating point takes, so it is taken in the precision of
- *     the CUDA library, on the same numbers (see nucleus_mass below); p' itself
- *     is computed in double.
+ *     T == 0 ignores both (the argmax is always kept).  The kept set is
+ *     decided on these definitions in double precision.  A float32
+ *     implementation may place the top-p edge one or more groups away from
+ *     it where a group's A lies within 1e-5 * S_K of P * S_K; the oracle
+ *     reports, per row, the range of cuts (in groups, relative to the exact
+ *     one) that such rounding can reach, and recomputes a request under any
+ *     cut of that range on request (see adjusted_row), so that a result
+ *     decided on the other side of such an edge can be checked too.
  *
  * Counter-based generator (the pages only say "uniform random"): SplitMix64
  * (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
@@ -175,79 +179,49 @@ static int by_logit_desc(const void* a, const void* b) {
   return (x->v > y->v) - (x->v < y->v);
 }
 
-/*
- * Masses on which the top-p edge is decided.  The pages fix no precision for
- * it; the CUDA library takes it in float32, so both sides take it on the same
- * float32 numbers, each from this written definition:
- *   c = log2(e) / T and z(v) = (M - L(v)) * c, in float32 (M = max L);
- *   2^-z = 0 when z >= 64 (or NaN); otherwise 2^-f * 2^-k with k = floor(z),
- *     f = z - k, and 2^-f the Taylor series sum_{n<=8} (-ln 2)^n f^n / n!
- *     (coefficients rounded to float32; Horner's rule with fused
- *     multiply-adds, highest power first);
- *   the mass of v is the integer round(2^-z * 2^F), F = 62 - ceil(log2 V), so
- *     that sums over a row are exact and do not depend on their order.
- * A(v) and S_K of the header comment are sums of these integers and the test
- * A(v) < P * S_K is evaluated in double as (double)A < (double)P * (double)S_K.
- * The series is within 4e-7 of 2^-f (relative).
- */
-static void pow2_neg_coefficients(float* a) {
-  double t = 1.0;
-  for (int n = 0; n <= 8; ++n) {
-    a[n] = (float)t;
-    t *= -log(2.0) / (double)(n + 1);
-  }
-}
-
-static float pow2_neg(float z, const float* a) {
-  if (!(z < 64.0f)) return 0.0f;
-  int k = (int)z;
-  float f = z - (float)k;
-  float q = a[8];
-  for (int n = 7; n >= 0; --n) q = fmaf(q, f, a[n]);
-  return ldexpf(q, -k);
-}
-
-/* Exported for the tests: 2^-z as defined above. */
-float oracle_pow2_neg(float z) {
-  float a[9];
-  pow2_neg_coefficients(a);
-  return pow2_neg(z, a);
-}
-
-static int mass_shift(int V) {
-  int lg = 0;
-  while ((1LL << lg) < (long long)V) ++lg;
-  return 62 - lg;
-}
-
-/* Exported for the tests: for j < n, the integer mass of an entry at distance
- * z[j] from the maximum of a row of V entries (as the top-p sums take it) into
- * mass[j], and 2^-z[j] into p2[j]. */
-void oracle_selection_mass(const float* z, int64_t n, int V, uint64_t* mass, float* p2) {
-  float a[9];
-  pow2_neg_coefficients(a);
-  const int F = mass_shift(V);
-  for (int64_t j = 0; j < n; ++j) {
-    const float q = pow2_neg(z[j], a);
-    p2[j] = q;
-    mass[j] = (uint64_t)nearbyintf(ldexpf(q, F));
-  }
-}
+/* Half-width of the band around the top-p bound, relative to the top-k mass
+ * S_K, inside which a float32 evaluation of the masses may decide a group
+ * boundary either way (the same relative margin as the accept-test and race
+ * near ties). */
+#define EDGE_BAND_REL 1e-5
 
 /*
  * The target distribution of one row after temperature, top-k and top-p (the
  * adjusted p of [P4] Section 2.2; the kept sets are defined in the header
- * comment).  top_k outside [1, V) and top_p >= 1 leave the softmax unchanged.
- * Returns 0, or ORACLE_OOM.
+ * comment), in double precision from the definition:
+ *   e(v) = exp((L(v) - M) / T), M the row maximum;
+ *   the tokens are ordered by logit, largest first, and grouped by equal
+ *   logits; top-k keeps the groups before the one that holds the k-th
+ *   largest logit, and that group whole;
+ *   top-p keeps group g of those when A_g = 0 or A_g < P * S_K, A_g the sum of
+ *   e over the groups before g and S_K the sum of e over the top-k groups
+ *   (A grows with g, so the kept groups are the first c*: the exact cut).
+ * shift moves the cut by that many groups (0: the definition).  It must lie
+ * in the range a float32 evaluation can reach, returned in *lo .. *hi: cut c
+ * is reachable when group c-1 could still be kept (A_{c-1} < P S_K + b, or
+ * c = 1) and group c could still be dropped (A_c >= P S_K - b, or c is past
+ * the last group), b = EDGE_BAND_REL * S_K.  Only 0 < P < 1 has a band: with
+ * P <= 0 (or NaN) every group after the first has A > 0 = the bound, which
+ * no rounding changes.  top_k outside [1, V) and top_p >= 1 leave the softmax
+ * unchanged (*lo = *hi = 0).
+ * Returns 0, ORACLE_OOM, or ORACLE_INVALID_ARG for a shift outside the range.
  */
 static int adjusted_row(const void* logits, int dtype, size_t row, int V, double T, int top_k,
-                        double top_p, double* p) {
+                        double top_p, int shift, int* lo, int* hi, double* p) {
   const int use_k = top_k >= 1 && top_k < V;
   const int use_p = !(top_p >= 1.0);
+  *lo = *hi = 0;
   softmax_row(logits, dtype, row, V, T, p);
-  if (!use_k && !use_p) return 0;
+  if (!use_k && !use_p) return shift == 0 ? 0 : ORACLE_INVALID_ARG;
   ranked_t* r = (ranked_t*)malloc(sizeof(ranked_t) * (size_t)V);
-  if (!r) return ORACLE_OOM;
+  int* gend = (int*)malloc(sizeof(int) * (size_t)V);     /* end (exclusive) of each group */
+  double* above = (double*)malloc(sizeof(double) * ((size_t)V + 1));  /* A_g */
+  if (!r || !gend || !above) {
+    free(r);
+    free(gend);
+    free(above);
+    return ORACLE_OOM;
+  }
   double mx = -INFINITY;
   for (int v = 0; v < V; ++v) {
     r[v].l = logit_at(logits, dtype, row * (size_t)V + (size_t)v);
@@ -261,49 +235,76 @@ static int adjusted_row(const void* logits, int dtype, size_t row, int V, double
     kend = top_k;
     while (kend < V && r[kend].l == r[top_k - 1].l) ++kend;
   }
-  /* top-p: walk the groups of equal logits inside K, on the integer masses */
-  int end = kend;
-  if (use_p) {
-    float a[9];
-    pow2_neg_coefficients(a);
-    const int F = mass_shift(V);
-    const float c = 1.4426950408889634f / (float)T;
-    const float m32 = (float)mx;
-    uint64_t s_k = 0;
-    for (int j = 0; j < kend; ++j)
-      s_k += (uint64_t)nearbyintf(ldexpf(pow2_neg((m32 - (float)r[j].l) * c, a), F));
-    const double bound = top_p * (double)s_k;
-    uint64_t above = 0;
-    int j = 0;
-    end = 0;
-    while (j < kend) {
-      int g = j;
-      uint64_t gm = 0;
-      while (g < kend && r[g].l == r[j].l) {
-        gm += (uint64_t)nearbyintf(ldexpf(pow2_neg((m32 - (float)r[g].l) * c, a), F));
-        ++g;
-      }
-      if (!(above == 0 || (double)above < bound)) break;
-      end = g;
-      above += gm;
-      j = g;
+  /* groups of equal logits inside K and the mass above each */
+  int G = 0;
+  above[0] = 0.0;
+  for (int j = 0; j < kend;) {
+    int g = j;
+    double gm = 0.0;
+    while (g < kend && r[g].l == r[j].l) {
+      gm += exp((r[g].l - mx) / T);
+      ++g;
     }
+    gend[G] = g;
+    above[G + 1] = above[G] + gm;
+    ++G;
+    j = g;
   }
+  int cut = G;
+  if (use_p) {
+    const double s_k = above[G];
+    const double bound = top_p > 0.0 ? top_p * s_k : 0.0;
+    int exact = G;
+    for (int g = 1; g < G; ++g)
+      if (!(above[g] < bound)) {
+        exact = g;
+        break;
+      }
+    int c_lo = exact, c_hi = exact;
+    if (top_p > 0.0) {
+      const double band = EDGE_BAND_REL * s_k;
+      while (c_lo > 1 && above[c_lo - 1] >= bound - band) --c_lo;
+      while (c_hi < G && above[c_hi] < bound + band) ++c_hi;
+    }
+    *lo = c_lo - exact;
+    *hi = c_hi - exact;
+    cut = exact + shift;
+    if (shift < *lo || shift > *hi) {
+      free(r);
+      free(gend);
+      free(above);
+      return ORACLE_INVALID_ARG;
+    }
+  } else if (shift != 0) {
+    free(r);
+    free(gend);
+    free(above);
+    return ORACLE_INVALID_ARG;
+  }
+  const int end = gend[cut - 1];
   /* zero the dropped tokens, renormalise over the kept ones */
   double kept = 0.0;
   for (int j = 0; j < end; ++j) kept += exp((r[j].l - mx) / T);
   for (int j = end; j < V; ++j) p[r[j].v] = 0.0;
   for (int j = 0; j < end; ++j) p[r[j].v] = exp((r[j].l - mx) / T) / kept;
   free(r);
+  free(gend);
+  free(above);
   return 0;
 }
 
-/* Exported for the tests: the adjusted distribution of one row of V logits. */
+/* Exported for the tests: the adjusted distribution of one row of V logits
+ * with its cut moved by `shift` groups, and the reachable range of shifts
+ * (lo / hi may be NULL). */
 int oracle_adjusted_probs(const void* row, int dtype, int V, double T, int top_k, double top_p,
-                          double* p) {
+                          int shift, double* p, int32_t* lo, int32_t* hi) {
   if (!row || !p || V <= 0 || !(T > 0.0)) return ORACLE_INVALID_ARG;
   if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
-  return adjusted_row(row, dtype, 0, V, T, top_k, top_p, p);
+  int l = 0, h = 0;
+  const int s = adjusted_row(row, dtype, 0, V, T, top_k, top_p, shift, &l, &h, p);
+  if (lo) *lo = l;
+  if (hi) *hi = h;
+  return s;
 }
 
 /* Greedy target token: first index of the largest stored value. */
@@ -330,6 +331,10 @@ static int argmax_row(const void* logits, int dtype, size_t row, int V) {
  *   draft  : the request's gamma draft probability rows [gamma, V]; ignored when
  *            T == 0; NULL at T > 0 means a one-hot drafter (q_i = [v == x_i])
  *   ids    : the gamma draft token ids
+ * top_k / top_p adjust every target row of the request (top_k outside [1, V)
+ * and top_p >= 1 switch them off; T == 0 ignores them).  edge_shift
+ * [gamma+1] (or NULL: all 0) moves each row's top-p cut by that many groups
+ * within the range the row reports (see adjusted_row).
  * Outputs (any may be NULL):
  *   tokens [gamma+1]  accepted drafts, then the correction / bonus token, then -1
  *   num_accepted [1]  n
@@ -339,35 +344,43 @@ static int argmax_row(const void* logits, int dtype, size_t row, int V) {
  *                     rejection, where it no longer affects the output)
  *   pos_near_tie [gamma]  accept-test near tie at that position
  *   near_tie [1]      request-level flag (tested positions or the race)
- * top_k / top_p adjust every target row of the request (top_k outside [1, V)
- * and top_p >= 1 switch them off; T == 0 ignores them).
- * Returns ORACLE_OK, ORACLE_BAD_DRAFT_ID or ORACLE_OOM.
+ *   edge_lo, edge_hi [gamma+1]  range of reachable top-p cut shifts of each
+ *                     row (0 / 0 without a band; rows the request never adjusts,
+ *                     such as a bonus row after a rejection, report 0 / 0)
+ * Returns ORACLE_OK, ORACLE_BAD_DRAFT_ID, ORACLE_OOM, or ORACLE_INVALID_ARG
+ * for an edge shift outside its row's range.
  */
 int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
                               const float* draft, const int32_t* ids, int V, double T, int top_k,
-                              double top_p, uint64_t seed, int32_t* tokens, int32_t* num_accepted,
-                              double* beta, double* p_x, double* q_x, int32_t* accept,
-                              int32_t* pos_near_tie, int32_t* near_tie) {
+                              double top_p, const int32_t* edge_shift, uint64_t seed,
+                              int32_t* tokens, int32_t* num_accepted, double* beta, double* p_x,
+                              double* q_x, int32_t* accept, int32_t* pos_near_tie,
+                              int32_t* near_tie, int32_t* edge_lo, int32_t* edge_hi) {
   int status = ORACLE_OK;
   int n = gamma;
   int req_tie = 0;
-  int* acc = (int*)calloc((size_t)(gamma > 0 ? gamma : 1), sizeof(int));
-  int* tie = (int*)calloc((size_t)(gamma > 0 ? gamma : 1), sizeof(int));
-  if (!acc || !tie) {
-    free(acc);
-    free(tie);
-    return ORACLE_OOM;
-  }
   int t = -1;
+  const size_t g1 = (size_t)gamma + 1;
+  int* acc = (int*)calloc(g1, sizeof(int));
+  int* tie = (int*)calloc(g1, sizeof(int));
+  int* elo = (int*)calloc(g1, sizeof(int));
+  int* ehi = (int*)calloc(g1, sizeof(int));
+  int* g = NULL;
+  double* p = NULL;
+  double* w = NULL;
+  float* onehot = NULL;
+  if (!acc || !tie || !elo || !ehi) {
+    status = ORACLE_OOM;
+    goto done;
+  }
 
   if (T == 0.0) {
     /* Greedy: the adjusted p and q of [P4] Section 2.2 are one-hot at the
      * target argmax and at the draft id. */
-    int* g = (int*)malloc(sizeof(int) * (size_t)(gamma + 1));
+    g = (int*)malloc(sizeof(int) * g1);
     if (!g) {
-      free(acc);
-      free(tie);
-      return ORACLE_OOM;
+      status = ORACLE_OOM;
+      goto done;
     }
     for (int i = 0; i <= gamma; ++i) g[i] = argmax_row(tgt, dtype, (size_t)i, V);
     for (int i = 0; i < gamma; ++i) {
@@ -384,23 +397,19 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
         break;
       }
     t = g[n];
-    free(g);
   } else {
-    double* p = (double*)malloc(sizeof(double) * (size_t)V);
-    if (!p) {
-      free(acc);
-      free(tie);
-      return ORACLE_OOM;
+    p = (double*)malloc(sizeof(double) * (size_t)V);
+    w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!p || !w) {
+      status = ORACLE_OOM;
+      goto done;
     }
     /* A one-hot drafter: q_i(v) = [v == x_i], materialised row by row. */
-    float* onehot = NULL;
     if (!draft && gamma > 0) {
       onehot = (float*)calloc((size_t)gamma * (size_t)V, sizeof(float));
       if (!onehot) {
-        free(p);
-        free(acc);
-        free(tie);
-        return ORACLE_OOM;
+        status = ORACLE_OOM;
+        goto done;
       }
       for (int i = 0; i < gamma; ++i)
         if (ids[i] >= 0 && ids[i] < V) onehot[(size_t)i * (size_t)V + (size_t)ids[i]] = 1.0f;
@@ -409,12 +418,11 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
     /* Accept test and beta at every draft position. */
     for (int i = 0; i < gamma; ++i) {
       const float* q = draft + (size_t)i * (size_t)V;
-      if (adjusted_row(tgt, dtype, (size_t)i, V, T, top_k, top_p, p) == ORACLE_OOM) {
-        free(onehot);
-        free(p);
-        free(acc);
-        free(tie);
-        return ORACLE_OOM;
+      const int s = adjusted_row(tgt, dtype, (size_t)i, V, T, top_k, top_p,
+                                 edge_shift ? edge_shift[i] : 0, &elo[i], &ehi[i], p);
+      if (s != 0) {
+        status = s;
+        goto done;
       }
       int x = ids[i];
       double px = 0.0, qx = 0.0;
@@ -436,9 +444,9 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
       acc[i] = (r < a);
       double hi = r > a ? r : a;
       tie[i] = fabs(r - a) <= NEAR_TIE_REL * hi;
-      double s = 0.0;
-      for (int v = 0; v < V; ++v) s += (p[v] < (double)q[v]) ? p[v] : (double)q[v];
-      if (beta) beta[i] = s;
+      double sum = 0.0;
+      for (int v = 0; v < V; ++v) sum += (p[v] < (double)q[v]) ? p[v] : (double)q[v];
+      if (beta) beta[i] = sum;
       if (p_x) p_x[i] = px;
       if (q_x) q_x[i] = qx;
     }
@@ -450,21 +458,11 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
     for (int i = 0; i < gamma && i <= n; ++i) req_tie |= tie[i];
 
     /* Correction (n < gamma) or bonus (n == gamma) distribution w. */
-    double* w = (double*)malloc(sizeof(double) * (size_t)V);
-    if (!w) {
-      free(onehot);
-      free(p);
-      free(acc);
-      free(tie);
-      return ORACLE_OOM;
-    }
-    if (adjusted_row(tgt, dtype, (size_t)n, V, T, top_k, top_p, p) == ORACLE_OOM) {
-      free(w);
-      free(onehot);
-      free(p);
-      free(acc);
-      free(tie);
-      return ORACLE_OOM;
+    const int s = adjusted_row(tgt, dtype, (size_t)n, V, T, top_k, top_p,
+                               edge_shift ? edge_shift[n] : 0, &elo[n], &ehi[n], p);
+    if (s != 0) {
+      status = s;
+      goto done;
     }
     if (n < gamma) {
       const float* q = draft + (size_t)n * (size_t)V;
@@ -495,9 +493,6 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
       }
     }
     if (k2 > -INFINITY && (k1 - k2) <= NEAR_TIE_REL * k1) req_tie = 1;
-    free(w);
-    free(p);
-    free(onehot);
   }
 
   if (tokens) {
@@ -511,8 +506,19 @@ int oracle_verify_request_adj(int64_t b, int gamma, const void* tgt, int dtype,
   if (pos_near_tie)
     for (int i = 0; i < gamma; ++i) pos_near_tie[i] = tie[i];
   if (near_tie) *near_tie = req_tie;
+  if (edge_lo)
+    for (int i = 0; i <= gamma; ++i) edge_lo[i] = elo[i];
+  if (edge_hi)
+    for (int i = 0; i <= gamma; ++i) edge_hi[i] = ehi[i];
+done:
   free(acc);
   free(tie);
+  free(elo);
+  free(ehi);
+  free(g);
+  free(p);
+  free(w);
+  free(onehot);
   return status;
 }
 
@@ -521,8 +527,9 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
                           const int32_t* ids, int V, double T, uint64_t seed, int32_t* tokens,
                           int32_t* num_accepted, double* beta, double* p_x, double* q_x,
                           int32_t* accept, int32_t* pos_near_tie, int32_t* near_tie) {
-  return oracle_verify_request_adj(b, gamma, tgt, dtype, draft, ids, V, T, 0, 1.0, seed, tokens,
-                                   num_accepted, beta, p_x, q_x, accept, pos_near_tie, near_tie);
+  return oracle_verify_request_adj(b, gamma, tgt, dtype, draft, ids, V, T, 0, 1.0, NULL, seed,
+                                   tokens, num_accepted, beta, p_x, q_x, accept, pos_near_tie,
+                                   near_tie, NULL, NULL);
 }
 
 /* ---------------------------------------------------------------------- */
@@ -534,14 +541,17 @@ int oracle_verify_request(int64_t b, int gamma, const void* tgt, int dtype, cons
  * (cu_num_draft_tokens): request b owns draft rows cu[b] .. cu[b+1]-1 and
  * target rows cu[b]+b .. cu[b+1]+b (gamma_b + 1 rows, the last one the bonus
  * row).  Output token slots follow the target rows.  Per-position outputs
- * follow the draft rows; near_tie is per request.  Any output may be NULL.
+ * follow the draft rows; near_tie is per request; edge_lo / edge_hi (the
+ * reachable top-p cut shifts, see adjusted_row) follow the target rows.  Any
+ * output may be NULL.
  */
 int oracle_rejection_sample_adj(const void* target_logits, int dtype, const float* draft_probs,
                                 const int32_t* draft_ids, const int32_t* cu, int B, int V, double T,
                                 const int32_t* top_k, const double* top_p, uint64_t seed,
                                 int32_t* out_tokens, int32_t* out_num_accepted, double* out_beta,
                                 double* out_p_x, double* out_q_x, int32_t* out_accept,
-                                int32_t* out_pos_near_tie, int32_t* out_near_tie) {
+                                int32_t* out_pos_near_tie, int32_t* out_near_tie,
+                                int32_t* out_edge_lo, int32_t* out_edge_hi) {
   if (B <= 0 || V <= 0 || !target_logits || !draft_ids || !cu) return ORACLE_INVALID_ARG;
   if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
   if (!(T >= 0.0) || isinf(T)) return ORACLE_INVALID_ARG;
@@ -558,11 +568,12 @@ int oracle_rejection_sample_adj(const void* target_logits, int dtype, const floa
     const float* dr = (T > 0.0 && draft_probs) ? draft_probs + (size_t)d0 * (size_t)V : NULL;
     int s = oracle_verify_request_adj(
         b, gamma, tgt, dtype, dr, draft_ids + d0, V, T, top_k ? top_k[b] : 0,
-        top_p ? top_p[b] : 1.0, seed, out_tokens ? out_tokens + t0 : NULL,
+        top_p ? top_p[b] : 1.0, NULL, seed, out_tokens ? out_tokens + t0 : NULL,
         out_num_accepted ? out_num_accepted + b : NULL, out_beta ? out_beta + d0 : NULL,
         out_p_x ? out_p_x + d0 : NULL, out_q_x ? out_q_x + d0 : NULL,
         out_accept ? out_accept + d0 : NULL, out_pos_near_tie ? out_pos_near_tie + d0 : NULL,
-        out_near_tie ? out_near_tie + b : NULL);
+        out_near_tie ? out_near_tie + b : NULL, out_edge_lo ? out_edge_lo + t0 : NULL,
+        out_edge_hi ? out_edge_hi + t0 : NULL);
     if (s == ORACLE_OOM) return s;
     if (s != ORACLE_OK) status = s;
   }
@@ -577,5 +588,6 @@ int oracle_rejection_sample(const void* target_logits, int dtype, const float* d
                             int32_t* out_pos_near_tie, int32_t* out_near_tie) {
   return oracle_rejection_sample_adj(target_logits, dtype, draft_probs, draft_ids, cu, B, V, T, NULL,
                                      NULL, seed, out_tokens, out_num_accepted, out_beta, out_p_x,
-                                     out_q_x, out_accept, out_pos_near_tie, out_near_tie);
+                                     out_q_x, out_accept, out_pos_near_tie, out_near_tie, NULL,
+                                     NULL);
 }

@@ -45,7 +45,7 @@ static_assert(kStatusOff % 256 == 0 && kKeysOff % 256 == 0 && kNaccOff % 256 == 
 }  // namespace
 
 // The scratch array.  In host code this name is only a stand-in: its device
-// address comes from cudaGetSymbolAddress, taken once per device below.
+// address comes from cudaGetSymbolAddress (below).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 namespace {
@@ -55,21 +55,29 @@ std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 std::atomic<uint64_t> g_epoch{0};
 
-// Device address of the scratch array on the current device (set up on the
-// first call per device).
-int scratch_on_current_device(unsigned char** out, int* sms) {
+// Device address of the scratch array on the current device.  It is looked up
+// on every call made outside stream capture (a host-side query), so that a
+// module loaded again after cudaDeviceReset is found at its new address; a
+// call made while `st` is capturing uses the address of the last call on this
+// device outside capture (a lookup may not be legal there), so the first call
+// on a device has to come before any capture.
+int scratch_on_current_device(cudaStream_t st, unsigned char** out, int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPECDEC_ERR_CUDA;
   if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SPECDEC_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return SPECDEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return SPECDEC_ERR_CUDA;
     }
     g_scratch_ptr[dev] = p;
+  } else if (!g_scratch_ptr[dev]) {
+    return SPECDEC_ERR_CUDA;
   }
   *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
   return SPECDEC_OK;
@@ -91,13 +99,23 @@ extern "C" int specdec_rejection_sample_noalloc(
 
   unsigned char* base = nullptr;
   int sms = 0;
-  int rc = scratch_on_current_device(&base, &sms);
-  if (rc != SPECDEC_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = scratch_on_current_device(st, &base, &sms);
+  if (rc != SPECDEC_OK) return rc;
   uint32_t* small = reinterpret_cast<uint32_t*>(base + kSmallOff);
-  // Counters left by an earlier call (or by an earlier call that failed part-way)
-  // must start at zero; status words need no clearing (each call has its epoch).
+  // Everything a call accumulates into starts at zero on its stream: the small
+  // block (error word, deferred count, work counter), the greedy argmax keys
+  // (T == 0) and the per-request slice counters of the race (T > 0).  A call
+  // that completes leaves the keys and the slice counters at zero itself; these
+  // clears also cover an earlier call that stopped part-way.  Status words need
+  // no clearing (each call tags them with its own epoch).
   if (cudaMemsetAsync(small, 0, kSmallBytes, st) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (T == 0.0f) {
+    if (cudaMemsetAsync(base + kKeysOff, 0, kRows * sizeof(uint64_t), st) != cudaSuccess)
+      return SPECDEC_ERR_CUDA;
+  } else if (cudaMemsetAsync(base + kRcountOff, 0, kBatch * sizeof(int32_t), st) != cudaSuccess) {
+    return SPECDEC_ERR_CUDA;
+  }
 
   Params P = {};
   P.logits = target_logits;

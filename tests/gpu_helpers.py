@@ -2,7 +2,7 @@
 (via the package's ctypes binding) and compare with the CPU oracle."""
 from __future__ import annotations
 
-import math
+import os
 
 import numpy as np
 import torch
@@ -53,25 +53,117 @@ def run_gpu_adj(verifier, w: Workload, top_k, top_p, extended: bool = True):
     return res
 
 
+# Near-tie statistics of every comparison in this process (printed at the end of
+# the session by conftest.py): label -> [flagged requests, their rows, all rows,
+# requests with an ambiguous top-p edge, those decided on a shifted cut].
+FLAG_LOG: dict = {}
+
+
+def _per_request(a, B):
+    if a is None:
+        return None
+    a = np.asarray(a.cpu() if hasattr(a, "cpu") else a)
+    return np.broadcast_to(a, (B,))
+
+
+def _match_shifted(w: Workload, g: dict, b: int, top_k, top_p, tokens: bool = True) -> bool:
+    """Request b of a top-p call whose rows have an ambiguous edge: the GPU's
+    outputs must be the oracle's outputs under some reachable cut of each row
+    (several kept sets are correct there).  Checks every position's accept
+    test, beta and p(x) against the reachable cuts of its row, then (with
+    `tokens`) the emitted tokens under reachable cuts of the rows before the
+    first rejection and of the row the extra token is drawn from."""
+    cu = w.cu.cpu().numpy().astype(np.int64)
+    d0, d1 = cu[b], cu[b + 1]
+    t0, gam = d0 + b, d1 - d0
+    tgt = to_numpy_logits(w.target_logits[t0:t0 + gam + 1])
+    q = None if w.draft_probs is None else w.draft_probs[d0:d1].cpu().numpy()
+    ids = w.draft_ids[d0:d1].cpu().numpy()
+    k, p = int(top_k[b]), float(top_p[b])
+    ranges = [oracle.adjusted_probs(tgt[i], w.T, k, p, with_range=True)[1] for i in range(gam + 1)]
+
+    def run(shift):
+        r = oracle.verify_request(int(b), tgt, q, ids, w.T, w.seed, top_k=k, top_p=p,
+                                  edge_shift=shift)
+        assert r.status in (0, oracle.BAD_DRAFT_ID)
+        return r
+
+    def position_ok(r, i):
+        if "accept" in g and r.pos_near_tie[i] == 0 and g["accept"][d0 + i] != r.accept[i]:
+            return False
+        if abs(g["beta"][d0 + i] - r.beta[i]) > BETA_TOL:
+            return False
+        return "p_x" not in g or abs(g["p_x"][d0 + i] - r.p_x[i]) <= PROB_TOL
+
+    ok_shifts = []
+    for i in range(gam):
+        good = []
+        for s in range(ranges[i][0], ranges[i][1] + 1):
+            sv = np.zeros(gam + 1, np.int32)
+            sv[i] = s
+            if position_ok(run(sv), i):
+                good.append(s)
+        if not good:
+            return False
+        ok_shifts.append(good)
+    if not tokens:
+        return True
+    n = int(g["num_accepted"][b])
+    shift = np.zeros(gam + 1, np.int32)
+    for i in range(n):
+        shift[i] = 0 if 0 in ok_shifts[i] else ok_shifts[i][0]
+    last = ok_shifts[n] if n < gam else list(range(ranges[gam][0], ranges[gam][1] + 1))
+    for s in last:
+        shift[n] = s
+        r = run(shift)
+        if r.num_accepted[0] == n and (r.near_tie[0] or
+                                       np.array_equal(g["tokens"][t0:t0 + gam + 1], r.tokens)):
+            return True
+    return False
+
+
 def compare(w: Workload, g: dict, r: oracle.OracleResult, exact: bool = False,
-            requests=None) -> dict:
+            requests=None, top_k=None, top_p=None, label: str | None = None) -> dict:
     """Element-by-element comparison.  Greedy (exact=True): everything
     bit-exact.  Sampling: tokens / counts identical on requests the oracle does
-    not flag as near ties, probabilities and beta within 1e-5."""
+    not flag as near ties, probabilities and beta within 1e-5.  Requests whose
+    top-p edge the oracle reports as ambiguous (top_k / top_p given) must match
+    the exact cut or, failing that, some reachable cut of each row."""
     cu = w.cu.cpu().numpy().astype(np.int64)
     B = len(cu) - 1
-    reqs = range(B) if requests is None else requests
-    flagged = 0
+    reqs = list(range(B) if requests is None else requests)
+    tk, tp = _per_request(top_k, B), _per_request(top_p, B)
+    flagged = flagged_rows = edge_req = edge_shifted = 0
+    skip_pos = []
     for b in reqs:
         d0, d1 = cu[b], cu[b + 1]
         t0, t1 = d0 + b, d1 + b + 1
-        if not exact and r.near_tie[b]:
+        tie = (not exact) and bool(r.near_tie[b])
+        if tie:
             flagged += 1
+            flagged_rows += int(t1 - t0)
+        amb = (not exact and r.edge_lo is not None and tp is not None
+               and bool(np.any(r.edge_lo[t0:t1] != 0) or np.any(r.edge_hi[t0:t1] != 0)))
+        same_tok = tie or (g["num_accepted"][b] == r.num_accepted[b]
+                           and np.array_equal(g["tokens"][t0:t1], r.tokens[t0:t1]))
+        if amb:
+            edge_req += 1
+            pos = np.arange(d0, d1)
+            same = same_tok and bool(np.all(np.abs(g["beta"][pos] - r.beta[pos]) <= BETA_TOL))
+            if "p_x" in g:
+                same = same and bool(np.all(np.abs(g["p_x"][pos] - r.p_x[pos]) <= PROB_TOL))
+                ok = r.pos_near_tie[pos] == 0
+                same = same and np.array_equal(g["accept"][pos][ok], r.accept[pos][ok])
+            if not same:
+                assert _match_shifted(w, g, b, tk, tp, tokens=not tie), \
+                    f"request {b}: no reachable top-p cut explains the result"
+                edge_shifted += 1
+            skip_pos.extend(range(d0, d1))
             continue
-        assert g["num_accepted"][b] == r.num_accepted[b], f"request {b}: n"
-        assert np.array_equal(g["tokens"][t0:t1], r.tokens[t0:t1]), f"request {b}: tokens"
-    d_all = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in reqs]) if len(cu) > 1 else []
-    d_all = np.asarray(d_all, np.int64)
+        assert tie or g["num_accepted"][b] == r.num_accepted[b], f"request {b}: n"
+        assert same_tok, f"request {b}: tokens"
+    d_all = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in reqs]) if reqs else []
+    d_all = np.setdiff1d(np.asarray(d_all, np.int64), np.asarray(skip_pos, np.int64))
     if d_all.size:
         if exact:
             assert np.array_equal(g["beta"][d_all], r.beta[d_all].astype(np.float32))
@@ -86,14 +178,67 @@ def compare(w: Workload, g: dict, r: oracle.OracleResult, exact: bool = False,
                 assert np.abs(g["q_x"][d_all] - r.q_x[d_all]).max() <= PROB_TOL
                 ok = r.pos_near_tie[d_all] == 0
                 assert np.array_equal(g["accept"][d_all][ok], r.accept[d_all][ok])
-    n_req = len(list(reqs))
-    return dict(flagged=flagged, requests=n_req)
+    n_rows = int(sum(cu[b + 1] - cu[b] + 1 for b in reqs))
+    st = dict(flagged=flagged, flagged_rows=flagged_rows, requests=len(reqs), rows=n_rows,
+              edge_requests=edge_req, edge_shifted=edge_shifted)
+    if label is None:
+        label = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    if label:
+        acc = FLAG_LOG.setdefault(label, [0, 0, 0, 0, 0])
+        for j, key in enumerate(("flagged", "flagged_rows", "rows", "edge_requests",
+                                 "edge_shifted")):
+            acc[j] += st[key]
+    return st
 
 
-def flag_budget_ok(flagged: int, n_requests: int) -> bool:
-    """Near-tie exemptions must stay under 0.01 % of rows (at least one allowed
-    on small batches)."""
-    return flagged <= max(1, math.ceil(1e-4 * n_requests))
+def flag_budget_ok(st: dict) -> bool:
+    """Rows of near-tie requests (exempt from token identity) must stay under
+    0.01 % of the rows compared."""
+    return st["flagged_rows"] < 1e-4 * st["rows"] or st["flagged_rows"] == 0
+
+
+def run_oracle_threaded(w: Workload, top_k=None, top_p=None, threads: int | None = None):
+    """The whole batch through the oracle, request by request (each request
+    keeps its own index as the generator key), on several host threads over
+    contiguous request ranges (the oracle's C calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = threads or max(1, min(32, os.cpu_count() or 1))
+    cu = w.cu.cpu().numpy().astype(np.int64)
+    n_t, n_d, B = w.n_target, w.n_draft, w.B
+    logits = to_numpy_logits(w.target_logits)
+    q_all = None if w.draft_probs is None else w.draft_probs.cpu().numpy()
+    ids_all = w.draft_ids.cpu().numpy()
+    tk, tp = _per_request(top_k, B), _per_request(top_p, B)
+    res = oracle.OracleResult(tokens=np.full(n_t, -2, np.int32), num_accepted=np.zeros(B, np.int32),
+                              beta=np.zeros(n_d), p_x=np.zeros(n_d), q_x=np.zeros(n_d),
+                              accept=np.zeros(n_d, np.int32), pos_near_tie=np.zeros(n_d, np.int32),
+                              near_tie=np.zeros(B, np.int32), status=0,
+                              edge_lo=np.zeros(n_t, np.int32), edge_hi=np.zeros(n_t, np.int32))
+    oracle.splitmix64(0)          # loads the library before the threads start
+
+    def work(part):
+        for b in range(part * B // threads, (part + 1) * B // threads):
+            d0, d1 = cu[b], cu[b + 1]
+            t0, t1 = d0 + b, d1 + b + 1
+            one = oracle.verify_request(int(b), logits[t0:t1], None if q_all is None else q_all[d0:d1],
+                                        ids_all[d0:d1], w.T, w.seed,
+                                        top_k=0 if tk is None else int(tk[b]),
+                                        top_p=1.0 if tp is None else float(tp[b]))
+            res.tokens[t0:t1] = one.tokens
+            res.num_accepted[b] = one.num_accepted[0]
+            res.beta[d0:d1] = one.beta
+            res.p_x[d0:d1] = one.p_x
+            res.q_x[d0:d1] = one.q_x
+            res.accept[d0:d1] = one.accept
+            res.pos_near_tie[d0:d1] = one.pos_near_tie
+            res.near_tie[b] = one.near_tie[0]
+            res.edge_lo[t0:t1] = one.edge_lo
+            res.edge_hi[t0:t1] = one.edge_hi
+            if one.status != 0:
+                res.status = one.status
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        list(pool.map(work, range(threads)))
+    return res
 
 
 def sampled_oracle(w: Workload, requests, top_k=None, top_p=None):
@@ -104,7 +249,8 @@ def sampled_oracle(w: Workload, requests, top_k=None, top_p=None):
     res = oracle.OracleResult(tokens=np.full(n_t, -2, np.int32), num_accepted=np.zeros(B, np.int32),
                               beta=np.zeros(n_d), p_x=np.zeros(n_d), q_x=np.zeros(n_d),
                               accept=np.zeros(n_d, np.int32), pos_near_tie=np.zeros(n_d, np.int32),
-                              near_tie=np.zeros(B, np.int32), status=0)
+                              near_tie=np.zeros(B, np.int32), status=0,
+                              edge_lo=np.zeros(n_t, np.int32), edge_hi=np.zeros(n_t, np.int32))
     tk = None if top_k is None else top_k.cpu().numpy()
     tp = None if top_p is None else top_p.cpu().numpy()
     for b in requests:
@@ -123,6 +269,8 @@ def sampled_oracle(w: Workload, requests, top_k=None, top_p=None):
         res.accept[d0:d1] = one.accept
         res.pos_near_tie[d0:d1] = one.pos_near_tie
         res.near_tie[b] = one.near_tie[0]
+        res.edge_lo[t0:t1] = one.edge_lo
+        res.edge_hi[t0:t1] = one.edge_hi
     return res
 
 

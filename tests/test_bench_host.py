@@ -66,16 +66,29 @@ def test_clock_sampler_median_and_reasons(tmp_path):
 def test_recorded_traffic_needs_current_source_and_workload(tmp_path, monkeypatch):
     path = tmp_path / "traffic.txt"
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
-    assert bench.recorded_traffic("w", "k") is None          # no record
+    assert bench.recorded_traffic("w", "k", 1000) is None          # no record
     h = bench.kernel_source_hash()
     path.write_text("# note: a comment with a colon\n"
                     f"kernel: k\nworkload_key: w\nsource_sha256_16: {h}\n"
-                    "traffic_bytes_per_launch: 123456\n")
-    assert bench.recorded_traffic("w", "k") == 123456.0
-    assert bench.recorded_traffic("other", "k") is None
-    assert bench.recorded_traffic("w", "other") is None
+                    "traffic_bytes_per_algorithmic_byte: 1.25\n")
+    # scaled to the algorithmic bytes of the launch being reported
+    assert bench.recorded_traffic("w", "k", 1000) == 1250.0
+    assert bench.recorded_traffic("w", "k", 8000) == 10000.0
+    assert bench.recorded_traffic("other", "k", 1000) is None
+    assert bench.recorded_traffic("w", "other", 1000) is None
     path.write_text(path.read_text().replace(h, "0" * 16))
-    assert bench.recorded_traffic("w", "k") is None          # taken on other kernel code
+    assert bench.recorded_traffic("w", "k", 1000) is None          # taken on other kernel code
+
+
+def test_secondary_workload_defaults():
+    # the plain large workload carries the ragged one beside it; anything else
+    # runs alone unless asked
+    assert bench.parse_args([]).secondary == 3
+    assert bench.parse_args(["--secondary", "-1"]).secondary is None
+    assert bench.parse_args(["--config", "3"]).secondary is None
+    assert bench.parse_args(["--top-k", "50"]).secondary is None
+    assert bench.parse_args(["--draft", "onehot"]).secondary is None
+    assert bench.parse_args(["--config", "2", "--secondary", "1"]).secondary == 1
 
 
 def _args(**kw):

@@ -7,7 +7,7 @@ import torch
 
 import stat_checks as sc
 from gpu_helpers import (compare, flag_budget_ok, run_gpu, run_gpu_adj, run_oracle,
-                         sampled_oracle)
+                         run_oracle_threaded)
 from speculative_decoding_rejection_decode_gb300.inputs import (from_rows, make_config,
                                                                 make_top_k_top_p, make_workload)
 
@@ -28,17 +28,19 @@ def _check(V, w, tk, tp, budget=True):
     g = run_gpu_adj(V, w, tk, tp)
     assert V.get_error() == 0
     r = run_oracle(w, tk, tp)
-    st = compare(w, g, r)
+    st = compare(w, g, r, top_k=tk, top_p=tp)
     if budget:
-        assert flag_budget_ok(st["flagged"], st["requests"]), st
+        assert flag_budget_ok(st), st
     return g, r
 
 
 @pytest.mark.parametrize("vocab", [1, 2, 3, 1000, 32000, 151936, 256000, 262145, 1 << 30])
-def test_selection_mass_bit_exact(V, vocab):
-    # the top-p masses (2^-z and its integer scaling) on the device equal the
-    # oracle's independent implementation of the same written definition
-    import oracle
+def test_selection_mass_accuracy(V, vocab):
+    # a unit test of the kernel's own top-p masses (the oracle decides the edge
+    # from exp in double and takes no part here): 2^-z within 4e-7 relative of
+    # 2^-z, exact powers of two at integer z, 0 from z = 64 on and for NaN; the
+    # integer mass is 2^-z scaled by 2^F, F = 62 - ceil(log2 V), rounded to the
+    # nearest integer, so that V of them never exceed 2^62
     from speculative_decoding_rejection_decode_gb300 import selection_mass
     rng = np.random.default_rng(vocab % 1000)
     ints = np.arange(0, 70, dtype=np.float32)
@@ -46,12 +48,19 @@ def test_selection_mass_bit_exact(V, vocab):
         rng.uniform(0, 70, 200000), rng.uniform(0, 1, 50000), rng.uniform(40, 64, 50000),
         ints, np.nextafter(ints, np.float32(np.inf)), np.nextafter(ints, np.float32(-np.inf))[1:],
         [-0.0, 63.99999, 64.0, 1e30, np.inf, np.nan]]).astype(np.float32)
-    want_m, want_p = oracle.selection_mass(z, vocab)
     got_m, got_p = selection_mass(torch.from_numpy(z).cuda(), vocab)
-    got_m = got_m.cpu().numpy().view(np.uint64)
-    got_p = got_p.cpu().numpy()
-    assert np.array_equal(got_p.view(np.uint32), want_p.view(np.uint32))
-    assert np.array_equal(got_m, want_m)
+    got_m = got_m.cpu().numpy().view(np.uint64).astype(np.float64)
+    got_p = got_p.cpu().numpy().astype(np.float64)
+    F = 62 - int(np.ceil(np.log2(vocab))) if vocab > 1 else 62
+    z64 = z.astype(np.float64)
+    live = np.isfinite(z64) & (z64 < 64)
+    ref = np.exp2(-z64[live])
+    assert np.all(np.abs(got_p[live] - ref) <= 4e-7 * ref)
+    assert np.all(got_p[~live] == 0) and np.all(got_m[~live] == 0)
+    at_int = live & (z64 == np.floor(z64)) & (z64 >= 0)
+    assert np.array_equal(got_p[at_int], np.exp2(-z64[at_int]))
+    assert np.all(np.abs(got_m[live] - got_p[live] * 2.0 ** F) <= 0.5)
+    assert vocab * got_m.max() <= 2.0 ** 62
 
 
 def test_selection_mass_argument_checks(V):
@@ -76,18 +85,20 @@ def test_large_vocab_bf16_uniform_settings(V, top_k, top_p):
     _check(V, w, tk, tp)
 
 
-def test_full_size_large_workload_sampled(V):
+def test_full_size_large_workload(V):
+    # the large workload at full size with the seeded per-request settings,
+    # against the oracle on every request (threads over request ranges)
     w = make_config(4, device="cuda")
     tk, tp = make_top_k_top_p(w.B, w.V, seed=44)
     g = run_gpu_adj(V, w, tk, tp)
     assert V.get_error() == 0
     cu = w.cu.cpu().numpy()
     sc.check_e_layout(g["tokens"], g["num_accepted"], w.draft_ids.cpu().numpy(), cu, w.V)
-    rng = np.random.default_rng(44)
-    reqs = sorted(set([0, 1, w.B - 1] + list(rng.choice(w.B, 9, replace=False))))
-    r = sampled_oracle(w, reqs, tk, tp)
-    st = compare(w, g, r, requests=reqs)
-    assert st["flagged"] <= 1
+    r = run_oracle_threaded(w, tk, tp)
+    assert r.status == 0
+    st = compare(w, g, r, top_k=tk, top_p=tp)
+    assert st["requests"] == w.B
+    assert flag_budget_ok(st), st
 
 
 @pytest.mark.parametrize("Vsz,dtype", [(8, "f32"), (8, "bf16"), (100, "f32"), (4097, "bf16"),

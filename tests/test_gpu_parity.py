@@ -10,7 +10,7 @@ import torch
 import oracle
 import stat_checks as sc
 from gpu_helpers import (compare, flag_budget_ok, numpy_runner, run_gpu, run_oracle,
-                         sampled_oracle)
+                         run_oracle_threaded)
 from speculative_decoding_rejection_decode_gb300.inputs import (from_rows, make_config,
                                                                 make_workload)
 
@@ -97,7 +97,7 @@ def test_config1(V, path):
     assert V.get_error() == 0
     assert V.last_path()[0] == _paths()[path]
     st = compare(w, g, run_oracle(w))
-    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert flag_budget_ok(st), st
     V.set_path(0)
 
 
@@ -123,28 +123,24 @@ def test_config3_ragged(V, path):
     if path == "fused":
         assert c == 4
     st = compare(w, g, run_oracle(w))
-    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert flag_budget_ok(st), st
     V.set_path(0)
 
 
-def test_config4_full_size_sampled(V):
+def test_config4_full_size(V):
+    # the large workload at full size, in the launch configuration the benchmark
+    # times, against the oracle on every request (threads over request ranges)
     w = make_config(4, device="cuda")
     g = run_gpu(V, w)
     assert V.get_error() == 0
     assert V.last_path()[0] == _paths()["sweep"]
     cu = w.cu.cpu().numpy()
-    # properties that hold for every request
     sc.check_e_layout(g["tokens"], g["num_accepted"], w.draft_ids.cpu().numpy(), cu, w.V)
-    assert np.all((g["beta"] > 0) & (g["beta"] <= 1 + 1e-6))
-    assert np.array_equal(g["accept"][np.concatenate([np.arange(cu[b], cu[b] + n) for b, n in
-                                                      enumerate(g["num_accepted"])])],
-                          np.ones(int(g["num_accepted"].sum()), np.int32))
-    # element-by-element against the oracle on sampled requests (first, last, spread)
-    rng = np.random.default_rng(4)
-    reqs = sorted(set([0, 1, w.B - 1] + list(rng.choice(w.B, 9, replace=False))))
-    r = sampled_oracle(w, reqs)
-    st = compare(w, g, r, requests=reqs)
-    assert st["flagged"] <= 1
+    r = run_oracle_threaded(w)
+    assert r.status == 0
+    st = compare(w, g, r)
+    assert st["requests"] == w.B and st["rows"] == w.n_target
+    assert flag_budget_ok(st), st
 
 
 @pytest.mark.parametrize("path", ALL_PATHS)
@@ -154,7 +150,7 @@ def test_config4_reduced_full_parity(V, path):
     g = run_gpu(V, w)
     assert V.get_error() == 0
     st = compare(w, g, run_oracle(w))
-    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert flag_budget_ok(st), st
     V.set_path(0)
 
 
@@ -183,7 +179,7 @@ def test_vocab_sizes_and_tails(V, Vsz, dtype, path):
     g = run_gpu(V, w)
     assert V.get_error() == 0
     st = compare(w, g, run_oracle(w))
-    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert flag_budget_ok(st), st
     V.set_path(0)
 
 
@@ -193,7 +189,7 @@ def test_temperatures(V, T):
                       target_std=3.0, noise_std=1.0, draft_T=T, device="cuda")
     g = run_gpu(V, w)
     st = compare(w, g, run_oracle(w))
-    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert flag_budget_ok(st), st
 
 
 def test_gamma_zero_and_empty_requests(V):
@@ -204,7 +200,7 @@ def test_gamma_zero_and_empty_requests(V):
         V.set_path(path)
         g = run_gpu(V, w)
         st = compare(w, g, run_oracle(w))
-        assert flag_budget_ok(st["flagged"], st["requests"])
+        assert flag_budget_ok(st), st
     V.set_path(0)
 
 
@@ -375,7 +371,7 @@ def test_onehot_drafts_parity(V, Vsz, dtype, T):
     assert V.get_error() == 0
     r = run_oracle(w)
     st = compare(w, g, r)
-    assert flag_budget_ok(st["flagged"], st["requests"])
+    assert flag_budget_ok(st), st
     assert np.all(g["q_x"] == 1.0)
     assert np.abs(g["beta"] - g["p_x"]).max() <= 1e-6      # beta = p(x)
 

@@ -3,7 +3,9 @@ page's Section 2.2 note folds top-k and top-p into the adjusted p before the
 same rejection test).  The kept set and its renormalisation are checked against
 hand values, against a token-by-token evaluation of the definition on tiny rows
 with planted ties, against the properties that make it the nucleus, and through
-the output distribution of the whole verify step."""
+the output distribution of the whole verify step.  The band of reachable cuts
+around the top-p edge (the group boundaries a float32 evaluation may decide the
+other way) is checked on rows built around its 1e-5 boundary."""
 import numpy as np
 import pytest
 
@@ -15,10 +17,10 @@ def _f32(x):
     return np.asarray(x, np.float32)
 
 
-def _near_edge(l, T, k, P, rel=1e-5):
+def _near_edge(l, T, k, P, rel=1e-12):
     """True when some group's larger-logit mass lies within `rel` of the top-p
-    bound in exact arithmetic: there the float32 decision of the edge may go
-    either way, so the exact definition is not a pin."""
+    bound: there a different order of the double sums may decide the edge
+    the other way, so the token-by-token evaluation is not a pin."""
     if P >= 1.0:
         return False
     l = np.asarray(l, np.float64)
@@ -31,45 +33,6 @@ def _near_edge(l, T, k, P, rel=1e-5):
         if a > 0 and abs(a - bound) <= rel * e[in_k].sum():
             return True
     return False
-
-
-def test_pow2_neg_definition():
-    # 2^-z on the float32 definition: 0 from z = 64 on, exact powers of two at
-    # integer z, within 4e-7 of 2^-z elsewhere
-    assert oracle.pow2_neg(0.0) == 1.0
-    for k in range(64):
-        assert oracle.pow2_neg(float(k)) == 2.0 ** -k
-    assert oracle.pow2_neg(64.0) == 0.0 and oracle.pow2_neg(1e30) == 0.0
-    assert oracle.pow2_neg(float("nan")) == 0.0
-    rng = np.random.default_rng(0)
-    z = np.concatenate([rng.uniform(0, 64, 20000), rng.uniform(0, 1, 20000)]).astype(np.float32)
-    got = np.array([oracle.pow2_neg(float(x)) for x in z])
-    rel = np.abs(got - np.exp2(-z.astype(np.float64))) / np.exp2(-z.astype(np.float64))
-    assert rel.max() < 4e-7, rel.max()
-    # monotone non-increasing in z on a fine grid of one unit
-    g = np.array([oracle.pow2_neg(float(x)) for x in np.linspace(3, 4, 5001, dtype=np.float32)])
-    assert np.all(np.diff(g) <= 0)
-
-
-def test_selection_mass_definition():
-    # the integer mass 2^-z * 2^F rounded to the nearest integer, ties to even,
-    # with F = 62 - ceil(log2 V): F from V's powers of two, exact powers of two
-    # at integer z, 1/2 rounds to 0 and 2^-1/2 to 1, nothing past z = 64, a row
-    # of V entries at the maximum sums to at most 2^62, and 2^-z as above
-    for V, F in [(1, 62), (2, 61), (3, 60), (4, 60), (5, 59), (32000, 47), (151936, 44),
-                 (256000, 44), (262144, 44), (262145, 43), (1 << 30, 32)]:
-        z = np.array([0.0, 1.0, 5.0, F - 1.0, float(F), F + 0.5, F + 1.0, F + 2.0, 64.0],
-                     np.float32)
-        mass, p2 = oracle.selection_mass(z, V)
-        assert mass.dtype == np.uint64
-        assert [int(m) for m in mass] == [2 ** F, 2 ** (F - 1), 2 ** (F - 5), 2, 1, 1, 0, 0, 0], V
-        assert V * int(mass[0]) <= 2 ** 62
-        assert np.array_equal(p2, np.array([oracle.pow2_neg(float(x)) for x in z], np.float32))
-    mass, _ = oracle.selection_mass(np.array([np.nan, np.inf, 1e30], np.float32), 1000)
-    assert mass.tolist() == [0, 0, 0]
-    # non-increasing in z
-    m, _ = oracle.selection_mass(np.linspace(0, 50, 20001, dtype=np.float32), 256000)
-    assert np.all(np.diff(m.astype(np.float64)) <= 0)
 
 
 def test_closed_forms():
@@ -227,3 +190,122 @@ def test_a_planted_tie_exclusive_cut_is_caught():
     assert np.allclose(got, want) and np.allclose(got, [0, 0.5, 0.5, 0])
     exclusive = np.array([0, 1.0, 0, 0])
     assert not np.allclose(exclusive, want)
+
+
+# ----------------------------------------------------------------------------
+# The band of reachable top-p cuts
+# ----------------------------------------------------------------------------
+
+NEAR = 0.6e-5
+FAR = 1.5e-5
+
+
+def _masses(l, T=1.0):
+    l = np.asarray(l, np.float64)
+    return np.exp((l - l.max()) / T)
+
+
+def _bound_at(l, g, rel, T=1.0):
+    """A top-p value that puts P * S at A_g (1 + rel): A_g the mass of the
+    first g groups of a row of distinct logits (largest first)."""
+    e = np.sort(_masses(l, T))[::-1]
+    a = e[:g].sum()
+    return a * (1.0 + rel) / e.sum()
+
+
+ROW = _f32(np.log([0.4, 0.3, 0.2, 0.1]))          # distinct logits, in order
+
+
+@pytest.mark.parametrize("rel,expect", [(+NEAR, (-1, 0)), (-NEAR, (0, 1)), (+FAR, (0, 0)),
+                                        (-FAR, (0, 0))])
+def test_band_around_one_boundary(rel, expect):
+    # P * S just above A_2 (the mass of groups 0 and 1): the exact cut keeps
+    # group 2 (A_2 < P S) and, within the band, dropping it is reachable.  Just
+    # below: the exact cut drops group 2 (A_2 >= P S) and keeping it is
+    # reachable.
+    P = _bound_at(ROW, 2, rel)
+    p, rng = oracle.adjusted_probs(ROW, 1.0, 0, P, with_range=True)
+    assert rng == expect
+    kept = (p > 0).sum()
+    assert kept == (3 if rel > 0 else 2)
+    for s in range(expect[0], expect[1] + 1):
+        ps = oracle.adjusted_probs(ROW, 1.0, 0, P, shift=s)
+        assert (ps > 0).sum() == kept + s
+        e = _masses(ROW)
+        keep = ps > 0
+        assert np.allclose(ps[keep], e[keep] / e[keep].sum(), rtol=1e-12, atol=0)
+    for s in (expect[0] - 1, expect[1] + 1):
+        with pytest.raises(ValueError):
+            oracle.adjusted_probs(ROW, 1.0, 0, P, shift=s)
+
+
+def test_band_spans_several_small_groups():
+    # many light groups right at the bound: every cut among them is reachable
+    light = [1e-6 * (1.06 - 0.01 * j) for j in range(6)]       # six distinct light logits
+    l = _f32(np.log([0.5, 0.5 - 6.3e-6] + light))
+    e = np.sort(_masses(l))[::-1]
+    P = (e[:2].sum() + 3 * e[2]) / e.sum()        # the bound in the middle of the light groups
+    p, (lo, hi) = oracle.adjusted_probs(l, 1.0, 0, P, with_range=True)
+    assert lo <= -2 and hi >= 2
+    base = (p > 0).sum()
+    for s in range(lo, hi + 1):
+        assert (oracle.adjusted_probs(l, 1.0, 0, P, shift=s) > 0).sum() == base + s
+
+
+def test_no_band_without_a_positive_top_p():
+    # top-k alone, P <= 0 and P >= 1 decide exactly: no shift is reachable
+    for k, P in [(2, 1.0), (0, 0.0), (0, -0.5), (3, 0.0), (0, 1.0), (0, float("nan"))]:
+        _, rng = oracle.adjusted_probs(ROW, 1.0, k, P, with_range=True)
+        assert rng == (0, 0), (k, P)
+        with pytest.raises(ValueError):
+            oracle.adjusted_probs(ROW, 1.0, k, P, shift=1)
+
+
+def test_band_is_relative_to_the_top_k_mass():
+    # with top-k = 3 the bound is P times the mass of the first three groups;
+    # a boundary within 1e-5 of it is in the band, one 1.5e-5 away is not
+    e = np.sort(_masses(ROW))[::-1]
+    for rel, expect in [(NEAR, (-1, 0)), (FAR, (0, 0))]:
+        P = e[:2].sum() * (1 + rel) / e[:3].sum()
+        _, rng = oracle.adjusted_probs(ROW, 1.0, 3, P, with_range=True)
+        assert rng == expect
+
+
+def test_request_under_a_shifted_cut():
+    # the accept test at position 0 depends on whether the draft token's group
+    # is kept: with the exact cut it is dropped (p'(x) = 0, rejected); with the
+    # reachable shift +1 it is kept and accepted (q(x) = p'(x) / 2 < p'(x))
+    P = _bound_at(ROW, 2, -NEAR)                  # group 2 (token 2) just dropped
+    tgt = np.stack([ROW, ROW]).astype(np.float32)
+    x = 2
+    p_kept = _masses(ROW)[:3] / _masses(ROW)[:3].sum()
+    q = np.full((1, 4), 0.0, np.float32)
+    q[0, x] = p_kept[x] / 2
+    q[0, 3] = 1 - q[0, x]
+    r0 = oracle.verify_request(0, tgt, q, [x], 1.0, 5, top_p=P)
+    assert r0.status == 0 and r0.accept[0] == 0 and r0.p_x[0] == 0
+    # row 0 is tested and drawn from; the bonus row is never adjusted (n = 0)
+    assert list(r0.edge_lo) == [0, 0] and list(r0.edge_hi) == [1, 0]
+    r1 = oracle.verify_request(0, tgt, q, [x], 1.0, 5, top_p=P, edge_shift=[1, 0])
+    assert r1.status == 0 and r1.accept[0] == 1
+    assert r1.p_x[0] == pytest.approx(p_kept[x], rel=1e-12)
+    assert r1.beta[0] == pytest.approx(np.minimum(np.r_[p_kept, 0], q[0]).sum(), rel=1e-12)
+    bad = oracle.verify_request(0, tgt, q, [x], 1.0, 5, top_p=P, edge_shift=[2, 0])
+    assert bad.status == oracle.INVALID_ARG
+
+
+def test_batch_reports_edge_ranges_per_target_row():
+    P = _bound_at(ROW, 2, NEAR)
+    tgt = np.stack([ROW] * 5).astype(np.float32)            # two requests: gamma 1 and 2
+    q = np.full((3, 4), 0.25, np.float32)
+    cu = np.array([0, 1, 3], np.int32)
+    r = oracle.rejection_sample(tgt, q, np.zeros(3, np.int32), cu, 1.0, 3, top_p=P)
+    assert r.status == 0
+    # every row the requests adjusted reports the same band; rows they never
+    # adjusted (a bonus row after a rejection) report none
+    for b in range(2):
+        t0, t1 = cu[b] + b, cu[b + 1] + b
+        n = r.num_accepted[b]
+        for t in range(t0, t1 + 1):
+            used = (t - t0) < (cu[b + 1] - cu[b]) or n == cu[b + 1] - cu[b]
+            assert (r.edge_lo[t], r.edge_hi[t]) == ((-1, 0) if used else (0, 0))

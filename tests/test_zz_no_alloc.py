@@ -8,7 +8,10 @@ device allocation after start-up.  Its scratch is a fixed device array shared
 by every call, so each check runs two calls in a row: the second must not see
 anything the first left behind.  Results must equal those of
 specdec_rejection_sample (same kernels) within the tolerance the other parity
-tests use (tokens and counts identical, beta within 1e-5)."""
+tests use (tokens and counts identical, beta within 1e-5), and, once, those of
+the CPU oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -29,6 +32,7 @@ def lib():
 
 
 def _handle_path(sd, w):
+    """The handle-based entry point on the path the allocation-free one runs."""
     v = sd.Verifier(0)
     if w.T > 0:
         v.set_path(sd.SPECDEC_PATH_SWEEP)
@@ -41,7 +45,7 @@ def _handle_path(sd, w):
     return res
 
 
-def _noalloc(sd, w, err):
+def _noalloc(sd, w, err, n_draft=None):
     wd = w.to("cuda")
     out_t = torch.full((w.n_target,), -7, dtype=torch.int32, device="cuda")
     out_n = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
@@ -50,7 +54,8 @@ def _noalloc(sd, w, err):
     rc = sd.specdec_rejection_sample_noalloc(
         wd.target_logits.data_ptr(), dtype,
         None if wd.draft_probs is None else wd.draft_probs.data_ptr(),
-        wd.draft_ids.data_ptr(), wd.cu.data_ptr(), w.B, w.V, w.T, w.seed, w.n_draft,
+        wd.draft_ids.data_ptr(), wd.cu.data_ptr(), w.B, w.V, w.T, w.seed,
+        w.n_draft if n_draft is None else n_draft,
         out_t.data_ptr(), out_n.data_ptr(), out_b.data_ptr(), err.data_ptr(),
         torch.cuda.current_stream().cuda_stream)
     assert rc == 0, sd.specdec_status_string(rc)
@@ -98,3 +103,47 @@ def test_noalloc_rejects_sizes_beyond_the_limit(lib):
             wd.draft_ids.data_ptr(), wd.cu.data_ptr(), B, w.V, 1.0, 0, nd, dummy.data_ptr(),
             dummy.data_ptr(), None, None, stream)
         assert rc == lib._lib.SPECDEC_ERR_CAPACITY
+
+
+def test_noalloc_matches_the_oracle(lib):
+    # the ragged workload at B = 60 against the CPU oracle, element by element
+    from gpu_helpers import compare, flag_budget_ok, run_oracle
+    w = make_config(3, device="cuda", B=60)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        tok, nacc, beta = _noalloc(lib, w, err)
+        st = compare(w, dict(tokens=tok, num_accepted=nacc, beta=beta), run_oracle(w))
+        assert flag_budget_ok(st), st
+    assert int(err.item()) == 0
+
+
+def test_noalloc_one_hot_drafts(lib):
+    # draft ids without draft rows at T > 0 (a one-hot drafter): the sweep
+    # kernel never reads a draft row
+    w = dataclasses.replace(make_config(2, device="cuda", B=48), T=1.0, seed=2)
+    assert w.draft_probs is None
+    ref = _handle_path(lib, w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        _same(_noalloc(lib, w, err), ref)
+    assert int(err.item()) == 0
+
+
+def test_noalloc_understated_positions_set_the_capacity_bit(lib):
+    # n_draft_positions below the real cu[B] passes the host check, but the
+    # real rows (16800) pass the limit: the kernels skip the rows past it and
+    # report SPECDEC_DEVERR_CAPACITY; a following well-formed call is clean
+    from speculative_decoding_rejection_decode_gb300._lib import SPECDEC_DEVERR_CAPACITY
+    from speculative_decoding_rejection_decode_gb300.inputs import make_workload
+    big = make_workload(name="over the row limit", B=2100, gamma=7, V=64, dtype="f32", T=1.0,
+                        seed=5, device="cuda")
+    assert big.n_target > lib._lib.SPECDEC_NOALLOC_MAX_ROWS
+    for T in (1.0, 0.0):
+        w = dataclasses.replace(big, T=T)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        _noalloc(lib, w, err, n_draft=1000)
+        assert int(err.item()) & SPECDEC_DEVERR_CAPACITY, T
+    w = make_config(1, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _same(_noalloc(lib, w, err), _handle_path(lib, w))
+    assert int(err.item()) == 0
