@@ -531,6 +531,11 @@ __device__ __forceinline__ void sweep2_4(const float* l, const float4& q4, float
       w[k] = (kHasQ && resid) ? fmaxf(p[k] - qv[k], 0.0f) : p[k];
       if (!kHasQ && (int)(v + k) == excl) w[k] = 0.0f;  // one-hot draft: residual is p without x
     }
+    if constexpr (kMask) {
+      // entries outside the adjusted row (and a zero residual) are no
+      // candidates: a group without any skips its four hashes
+      if (!((w[0] > 0.0f) | (w[1] > 0.0f) | (w[2] > 0.0f) | (w[3] > 0.0f))) return;
+    }
     race_offer4(best, w, rkey, v);
   }
 }
@@ -541,7 +546,7 @@ template <typename TT, int NT, bool kHasQ, bool kRace, bool kMask = false>
 __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo, int hi, bool vec,
                                        float M, float c, float invS, float tau, bool resid,
                                        uint64_t rkey, uint64_t pol, float& beta, Race& best,
-                                       int excl = -1) {
+                                       int excl = -1, bool sparse = false) {
   constexpr int kEl = 16 / sizeof(TT);
   // target vectors loaded per iteration: fewer where the race needs registers
   constexpr int U = kRace ? 2 : (sizeof(TT) == 2 ? 3 : 4);
@@ -557,6 +562,76 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
     // every lane of the warp (j = jw .. jw + 31) has a full step: j + lag is the
     // warp's last j.  What is left goes through the one-vector loop below.
     const int lag = kRace ? 31 - (tid & 31) : 0;
+    if (kMask && !kRace && sparse) {
+      // Adjusted rows that keep few entries: entries below tau have p' = 0, so
+      // they add nothing to beta and are no race candidates.  A target vector
+      // with no entry at or above tau is skipped whole, and its draft entries
+      // are never loaded (a top-k row of V = 256000 keeps a few dozen entries:
+      // nearly the whole draft row stays unread).  Skipping only drops
+      // additions of zero, so the sums are the same as without the test.  Rows
+      // that keep many entries, and the race (whose registers this loop's
+      // would spill), take the loop below, whose draft loads do not wait for
+      // the target vectors.
+      constexpr int U2 = 2;
+      for (; j + lag + (U2 - 1) * NT < nv; j += U2 * NT) {
+        if constexpr (kRace) {
+          if ((++round & 3) == 0) warp_race(best);
+        }
+        uint4 a[U2];
+#pragma unroll
+        for (int u = 0; u < U2; ++u) a[u] = ldg_hint(rv + j + u * NT, pol);
+        bool keep[U2];
+#pragma unroll
+        for (int u = 0; u < U2; ++u) {
+          float x[kEl];
+          unpack16<TT>(a[u], x);
+          keep[u] = false;
+#pragma unroll
+          for (int e = 0; e < kEl; ++e) keep[u] |= x[e] >= tau;
+        }
+        uint4 b[U2][kEl / 4];
+        if constexpr (kHasQ) {
+#pragma unroll
+          for (int u = 0; u < U2; ++u)
+            if (keep[u]) {
+#pragma unroll
+              for (int h = 0; h < kEl / 4; ++h) b[u][h] = ldg_hint(qv + (j + u * NT) * (kEl / 4) + h, pol);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U2; ++u) {
+          if (!keep[u]) continue;
+          float x[kEl];
+          unpack16<TT>(a[u], x);
+#pragma unroll
+          for (int h = 0; h < kEl / 4; ++h) {
+            float4 q4 = zero4;
+            if constexpr (kHasQ) q4 = *reinterpret_cast<const float4*>(&b[u][h]);
+            sweep2_4<kHasQ, kRace, kMask>(x + 4 * h, q4, M, c, invS, tau, resid, rkey,
+                                          (uint32_t)((j + u * NT) * kEl + 4 * h), beta, best, excl);
+          }
+        }
+      }
+      for (; j < nv; j += NT) {
+        float x[kEl];
+        unpack16<TT>(ldg_hint(rv + j, pol), x);
+        bool keep = false;
+#pragma unroll
+        for (int e = 0; e < kEl; ++e) keep |= x[e] >= tau;
+        if (!keep) continue;
+#pragma unroll
+        for (int h = 0; h < kEl / 4; ++h) {
+          float4 q4 = zero4;
+          if constexpr (kHasQ) {
+            uint4 w = ldg_hint(qv + j * (kEl / 4) + h, pol);
+            q4 = *reinterpret_cast<const float4*>(&w);
+          }
+          sweep2_4<kHasQ, kRace, kMask>(x + 4 * h, q4, M, c, invS, tau, resid, rkey,
+                                        (uint32_t)(j * kEl + 4 * h), beta, best, excl);
+        }
+      }
+      return;
+    }
     for (; j + lag + (U - 1) * NT < nv; j += U * NT) {
       if constexpr (kRace) {
         // every few rounds each lane takes the warp's best so far, so the
@@ -773,9 +848,14 @@ __device__ __forceinline__ int adj_bin1(float z, const AdjGrid& g) {
 }
 
 // Visits every entry of the row (or, with kSampled, one 16-byte vector in 16,
-// one element in 16 on unaligned rows) through f(x).
-template <typename TT, int NT, bool kSampled, typename Fn>
-__device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64_t pol, Fn&& f) {
+// one element in 16 on unaligned rows) through f(x), and calls g() after each
+// vector (each element on unaligned rows).
+struct AdjNoFlush {
+  __device__ __forceinline__ void operator()() const {}
+};
+template <typename TT, int NT, bool kSampled, typename Fn, typename Gn = AdjNoFlush>
+__device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64_t pol, Fn&& f,
+                                          Gn&& g = Gn()) {
   constexpr int kEl = 16 / sizeof(TT);
   constexpr int kStep = kSampled ? kAdjSample : 1;
   const int tid = threadIdx.x;
@@ -796,13 +876,17 @@ __device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64
         unpack16<TT>(cur, x);
 #pragma unroll
         for (int e = 0; e < kEl; ++e) f(x[e]);
+        g();
         if (jn >= nv) break;
         cur = nxt;
         j = jn;
       }
     }
   } else {
-    for (int v = tid * kStep; v < V; v += NT * kStep) f(load_logit(row + v));
+    for (int v = tid * kStep; v < V; v += NT * kStep) {
+      f(load_logit(row + v));
+      g();
+    }
   }
 }
 
@@ -898,14 +982,16 @@ template <typename TT, int NT>
 __device__ bool adj_refine(const TT* row, int V, bool vec, float M, float c, float fscale,
                            bool by_mass, uint32_t need, double bound, uint32_t above_c,
                            unsigned long long above_m, uint32_t lo, uint32_t hi,
-                           unsigned long long m_sel, uint64_t pol, AdjShared& A, uint32_t& key,
-                           unsigned long long& kept, unsigned long long* ctr) {
+                           unsigned long long m_sel, uint32_t c_sel, uint64_t pol, AdjShared& A,
+                           uint32_t& key, unsigned long long& kept, uint32_t& kept_cnt,
+                           unsigned long long* ctr) {
   const int tid = threadIdx.x;
   if (lo > hi) return false;
   for (int level = 0; level <= kAdjMaxKeyLevels; ++level) {
     if (lo == hi) {
       key = lo;
       kept = above_m + m_sel;
+      kept_cnt = above_c + c_sel;
       return true;
     }
     const uint32_t w = (uint32_t)(((unsigned long long)hi - lo + kAdjBins2) / kAdjBins2);
@@ -936,6 +1022,7 @@ __device__ bool adj_refine(const TT* row, int V, bool vec, float M, float c, flo
       lo = A.kmin2[s];
       hi = A.kmax2[s];
       m_sel = A.mass2[s];
+      c_sel = A.cnt2[s];
     }
     __syncthreads();
     if (s >= kAdjBins2 || lo > hi) return false;
@@ -952,7 +1039,7 @@ template <typename TT, int NT>
 __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float fscale, int top_k,
                         float top_p, bool use_k, bool use_p, const AdjGrid& g, uint64_t pol,
                         AdjShared& A, uint32_t& key, unsigned long long& kept,
-                        unsigned long long* ctr) {
+                        uint32_t& kept_cnt, unsigned long long* ctr) {
   const int tid = threadIdx.x;
   for (int j = tid; j < kAdjBins1; j += NT) {
     A.cnt1[j] = 0u;
@@ -961,14 +1048,20 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
     A.kmax1[j] = 0u;
   }
   __syncthreads();
-  // the far entries' mass matters only for a top-p bound over the whole row
+  // The far entries' mass matters only for a top-p bound over the whole row.
+  // Each far entry's 2^-z comes from the special-function unit (relative error
+  // below 2^-22) and is summed in float32 over one vector (at most 8 terms),
+  // then added as an integer: the sum is within 1e-6 relative of the exact one,
+  // which decides the edge the same way everywhere outside the 1e-5 band the
+  // oracle reports.
   const bool far_mass = use_p && !use_k;
   unsigned long long fm = 0;
+  float fv = 0.0f;
   adj_visit<TT, NT, false>(row, V, vec, pol, [&](float x) {
     const float z = (M - x) * c;
     const int b = adj_bin1(z, g);
     if (b < 0) {
-      if (far_mass) fm += adj_mass(z, fscale);
+      if (far_mass && z < 64.0f) fv += ex2(-z);  // NaN and z >= 64 add nothing
       return;
     }
     const uint32_t k = order_key(x);
@@ -976,6 +1069,11 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
     atomicAdd(&A.mass1[b], adj_mass(z, fscale));
     atomicMin(&A.kmin1[b], k);
     atomicMax(&A.kmax1[b], k);
+  }, [&]() {
+    if (far_mass) {
+      fm += __float2ull_rn(fv * fscale);
+      fv = 0.0f;
+    }
   });
   __syncthreads();
   unsigned long long tm = fm;
@@ -989,7 +1087,7 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
         by_mass ? (top_p > 0.0f ? (double)top_p : 0.0) * (double)kept : 0.0;
     adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, (uint32_t)top_k, bound, 0ull, A);
     const int j1 = A.sel;
-    uint32_t ac = 0, lo = 1, hi = 0;
+    uint32_t ac = 0, lo = 1, hi = 0, cs = 0;
     unsigned long long am = 0, ms = 0;
     if (j1 < kAdjBins1) {
       ac = A.ex_cnt;
@@ -997,10 +1095,11 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
       lo = A.kmin1[j1];
       hi = A.kmax1[j1];
       ms = A.mass1[j1];
+      cs = A.cnt1[j1];
     }
     __syncthreads();
     if (!adj_refine<TT, NT>(row, V, vec, M, c, fscale, by_mass, (uint32_t)top_k, bound, ac, am,
-                            lo, hi, ms, pol, A, key, kept, ctr))
+                            lo, hi, ms, cs, pol, A, key, kept, kept_cnt, ctr))
       return false;
   }
   return true;
@@ -1059,26 +1158,27 @@ __device__ bool adj_estimate(const TT* row, int V, bool vec, float M, float c, f
   return true;
 }
 
-// Threshold tau (keep l >= tau) and kept mass S of an adjusted row whose max is
-// M; S holds the row's softmax sum on entry.  Block-wide (every thread of the
-// block calls it with the same arguments).  Returns false, leaving tau and S
-// alone, when no threshold exists (NaN rows).
+// Threshold tau (keep l >= tau), kept mass S and number of kept entries of an
+// adjusted row whose max is M; S holds the row's softmax sum on entry.
+// Block-wide (every thread of the block calls it with the same arguments).
+// Returns false, leaving tau, S and kept_cnt alone, when no threshold exists
+// (NaN rows).
 template <typename TT, int NT>
 __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M, float c, int top_k,
                            float top_p, bool use_k, bool use_p, uint64_t pol, AdjShared& A,
-                           float& tau, float& S, unsigned long long* ctr) {
+                           float& tau, float& S, uint32_t& kept_cnt, unsigned long long* ctr) {
   // masses are pow2_neg(z) * 2^F with V * 2^F <= 2^62
   const int F = adj_mass_shift(V);
   const float fscale = adj_mass_scale(F);
   const double unscale = __longlong_as_double((long long)(1023 - F) << 52);
-  uint32_t key = 0u;
+  uint32_t key = 0u, kc = kept_cnt;
   unsigned long long kept = 0ull;
   AdjGrid g{64.0f, 0.0f, true};
   bool ok = false;
   adj_count(ctr, kAdjRows);
   if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g)) {
     ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, g, pol, A, key,
-                         kept, ctr);
+                         kept, kc, ctr);
     if (!ok) adj_count(ctr, kAdjMiss);
   } else {
     adj_count(ctr, kAdjTail);
@@ -1086,7 +1186,7 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
   if (!ok) {
     const AdjGrid full{64.0f, 0.0f, true};
     ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, full, pol, A, key,
-                         kept, ctr);
+                         kept, kc, ctr);
   }
   if (!ok) {
     adj_count(ctr, kAdjNone);
@@ -1094,6 +1194,7 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
   }
   tau = key_value(key);
   S = (float)((double)kept * unscale);
+  kept_cnt = kc;
   return true;
 }
 
@@ -1198,14 +1299,18 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     float M = -INFINITY, S = 0.0f;
     for (int w = 0; w < NW; ++w) softmax_merge(M, S, red[par][w].x, red[par][w].y, P.c);
     float tau = -INFINITY;
+    uint32_t kept_cnt = (uint32_t)V;
     if constexpr (kAdj) {
       const int kk = P.topk ? __ldg(P.topk + b) : 0;
       const float pp = P.topp ? __ldg(P.topp + b) : 1.0f;
       const bool use_k = kk >= 1 && kk < V, use_p = !(pp >= 1.0f);
       if ((use_k || use_p) && M > -INFINITY && M < INFINITY)
         adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, keep,
-                           *reinterpret_cast<AdjShared*>(adj_smem), tau, S, P.adj_ctr);
+                           *reinterpret_cast<AdjShared*>(adj_smem), tau, S, kept_cnt, P.adj_ctr);
     }
+    // few kept entries: at most 1/8 of the 16-byte vectors hold one, so sweep 2
+    // skips the others (and their draft entries) instead of streaming them
+    const bool sparse = kAdj && vec && (uint64_t)kept_cnt * (uint64_t)(8 * kEl) <= (uint64_t)V;
     const float invS = 1.0f / S;
 
     // ---- accept test (thread 0) and the race decision --------------------
@@ -1237,13 +1342,13 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     Race best = race_none();
     if (has_q && !onehot && race)
       sweep2<TT, NT, true, true, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
-                                       beta, best);
+                                       beta, best, -1, sparse);
     else if (has_q && !onehot)
       sweep2<TT, NT, true, false, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
-                                        beta, best);
+                                        beta, best, -1, sparse);
     else if (race)
       sweep2<TT, NT, false, true, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
-                                        beta, best, resid ? s_x : -1);
+                                        beta, best, resid ? s_x : -1, sparse);
     beta = warp_sum(beta);
     warp_race(best);
     if (lane == 0) red[par ^ 1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
