@@ -831,10 +831,14 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // Level-1 geometry: bins of width 1/scale in z (scale a power of two).  With
 // catch_all the last bin also takes every z past the grid, NaN included;
 // otherwise only z < cut is binned and the rest is "far".
+// With lo > 0 (top-p alone, when the sample pins the edge down) the bins cover
+// only the window [lo, cut): entries with z < lo lie above the edge, so only
+// their count and mass are needed, and those are summed in registers.
 struct AdjGrid {
   float scale;
   float cut;
   bool catch_all;
+  float lo;
 };
 
 __device__ __forceinline__ int adj_bin1(float z, const AdjGrid& g) {
@@ -843,7 +847,8 @@ __device__ __forceinline__ int adj_bin1(float z, const AdjGrid& g) {
     return y < (float)(kAdjBins1 - 1) ? (int)y : kAdjBins1 - 1;
   }
   if (!(z < g.cut)) return -1;
-  const int b = (int)(z * g.scale);
+  if (z < g.lo) return -2;
+  const int b = (int)((z - g.lo) * g.scale);  // monotone in z, so in the logit
   return b < kAdjBins1 ? b : kAdjBins1 - 1;  // the cut lies inside the grid; guard only
 }
 
@@ -1054,12 +1059,20 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
   // then added as an integer: the sum is within 1e-6 relative of the exact one,
   // which decides the edge the same way everywhere outside the 1e-5 band the
   // oracle reports.
+  // Entries above a window (z < g.lo) are counted and their masses summed the
+  // same way, apart from the far ones.
   const bool far_mass = use_p && !use_k;
-  unsigned long long fm = 0;
-  float fv = 0.0f;
+  unsigned long long fm = 0, um = 0;
+  uint32_t uc = 0;
+  float fv = 0.0f, uv = 0.0f;
   adj_visit<TT, NT, false>(row, V, vec, pol, [&](float x) {
     const float z = (M - x) * c;
     const int b = adj_bin1(z, g);
+    if (b == -2) {
+      ++uc;
+      uv += ex2(-z);
+      return;
+    }
     if (b < 0) {
       if (far_mass && z < 64.0f) fv += ex2(-z);  // NaN and z >= 64 add nothing
       return;
@@ -1074,24 +1087,35 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
       fm += __float2ull_rn(fv * fscale);
       fv = 0.0f;
     }
+    if (g.lo > 0.0f) {
+      um += __float2ull_rn(uv * fscale);
+      uv = 0.0f;
+    }
   });
   __syncthreads();
-  unsigned long long tm = fm;
+  unsigned long long tm = fm + um;
   for (int j = tid; j < kAdjBins1; j += NT) tm += A.mass1[j];
   kept = adj_block_sum<NT>(tm, A);
+  const unsigned long long above_m = g.lo > 0.0f ? adj_block_sum<NT>(um, A) : 0ull;
+  const uint32_t above_c = g.lo > 0.0f ? (uint32_t)adj_block_sum<NT>(uc, A) : 0u;
   key = 0u;  // below every logit
   for (int pass = 0; pass < 2; ++pass) {
     const bool by_mass = pass == 1;
     if (by_mass ? !use_p : !use_k) continue;
     const double bound =
         by_mass ? (top_p > 0.0f ? (double)top_p : 0.0) * (double)kept : 0.0;
-    adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, (uint32_t)top_k, bound, 0ull, A);
+    // the edge must lie in the window: the entries above it must not reach
+    // the bound (the first group, A = 0, is kept regardless)
+    if (above_c > 0 && (by_mass ? (double)above_m >= bound : above_c >= (uint32_t)top_k))
+      return false;
+    adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, (uint32_t)top_k - above_c, bound, above_m,
+                   A);
     const int j1 = A.sel;
     uint32_t ac = 0, lo = 1, hi = 0, cs = 0;
     unsigned long long am = 0, ms = 0;
     if (j1 < kAdjBins1) {
-      ac = A.ex_cnt;
-      am = A.ex_mass;
+      ac = A.ex_cnt + above_c;
+      am = A.ex_mass + above_m;
       lo = A.kmin1[j1];
       hi = A.kmax1[j1];
       ms = A.mass1[j1];
@@ -1115,7 +1139,7 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
 template <typename TT, int NT>
 __device__ bool adj_estimate(const TT* row, int V, bool vec, float M, float c, float S,
                              int top_k, float top_p, bool use_k, bool use_p, uint64_t pol,
-                             AdjShared& A, AdjGrid& g) {
+                             AdjShared& A, AdjGrid& g, AdjGrid& gw) {
   const int tid = threadIdx.x;
   const AdjGrid coarse{64.0f, 0.0f, true};
   for (int j = tid; j < kAdjBins1; j += NT) A.cnt1[j] = 0u;
@@ -1148,13 +1172,28 @@ __device__ bool adj_estimate(const TT* row, int V, bool vec, float M, float c, f
   __syncthreads();
   if (j >= kAdjBins1 - 1) return false;
   const float z_est = (float)(j + 1) * (1.0f / 64.0f);
+  // finest power-of-two bin width whose 2048 bins still cover [lo, cut)
+  auto fit = [](AdjGrid& q) {
+    const float span = q.cut - q.lo;
+    int a = 6;
+    while (a < 24 && (float)kAdjBins1 / (float)(1 << (a + 1)) >= span) ++a;
+    while (a > -8 && (float)kAdjBins1 * exp2f((float)-a) < span) --a;
+    q.scale = exp2f((float)a);
+    q.catch_all = false;
+  };
   g.cut = 1.0625f * z_est + 0.5f;
-  // finest power-of-two bin width whose 2048 bins still cover the cut
-  int a = 6;
-  while (a < 24 && (float)kAdjBins1 / (float)(1 << (a + 1)) >= g.cut) ++a;
-  while (a > -8 && (float)kAdjBins1 * exp2f((float)-a) < g.cut) --a;
-  g.scale = exp2f((float)a);
-  g.catch_all = false;
+  g.lo = 0.0f;
+  fit(g);
+  gw = g;
+  if (!use_k && top_p >= 0.7f) {
+    // The sample's tail mass pins a top-p edge with P >= 0.7 down to a few
+    // hundredths of a unit of z (the tail holds many light entries): the
+    // window grid bins only a band around it.
+    const float m = 0.3125f + 0.03125f * z_est;
+    gw.cut = z_est + m;
+    gw.lo = fmaxf(z_est - m, 0.0f);
+    fit(gw);
+  }
   return true;
 }
 
@@ -1173,12 +1212,17 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
   const double unscale = __longlong_as_double((long long)(1023 - F) << 52);
   uint32_t key = 0u, kc = kept_cnt;
   unsigned long long kept = 0ull;
-  AdjGrid g{64.0f, 0.0f, true};
+  AdjGrid g{64.0f, 0.0f, true}, gw{64.0f, 0.0f, true};
   bool ok = false;
   adj_count(ctr, kAdjRows);
-  if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g)) {
-    ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, g, pol, A, key,
-                         kept, kc, ctr);
+  if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g, gw)) {
+    // the window grid first (when the sample gave one), then the cut grid
+    if (gw.lo > 0.0f)
+      ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, gw, pol, A, key,
+                           kept, kc, ctr);
+    if (!ok)
+      ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, g, pol, A, key,
+                           kept, kc, ctr);
     if (!ok) adj_count(ctr, kAdjMiss);
   } else {
     adj_count(ctr, kAdjTail);
