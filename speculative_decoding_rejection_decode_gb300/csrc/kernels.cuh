@@ -895,6 +895,40 @@ __device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64
   }
 }
 
+// Visits every entry of the row through f(x, n), a vector at a time: n = kEl
+// values of one 16-byte vector, or n = 1 on unaligned rows.
+template <typename TT, int NT, typename Fn>
+__device__ __forceinline__ void adj_visit_vec(const TT* row, int V, bool vec, uint64_t pol, Fn&& f) {
+  constexpr int kEl = 16 / sizeof(TT);
+  const int tid = threadIdx.x;
+  if (vec) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    const int nv = V / kEl;
+    int j = tid;
+    if (j < nv) {
+      uint4 cur = ldg_hint(rv + j, pol);
+#pragma unroll 1
+      for (;;) {
+        const int jn = j + NT;
+        uint4 nxt = cur;
+        if (jn < nv) nxt = ldg_hint(rv + jn, pol);
+        float x[kEl];
+        unpack16<TT>(cur, x);
+        f(x, kEl);
+        if (jn >= nv) break;
+        cur = nxt;
+        j = jn;
+      }
+    }
+  } else {
+    for (int v = tid; v < V; v += NT) {
+      float x[kEl];
+      x[0] = load_logit(row + v);
+      f(x, 1);
+    }
+  }
+}
+
 // First bin j of [0, n) (bins run from the largest logits down) at which
 //   by count: the running count through j reaches `need`;
 //   by mass:  cnt[j] > 0 and above + the running mass through j >= bound.
@@ -1061,43 +1095,55 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
   // oracle reports.
   // Entries above a window (z < g.lo) are counted and their masses summed the
   // same way, apart from the far ones.
+  // Each vector is classified first; the atomics of its window entries follow
+  // in one loop, so a warp issues them about as often as its busiest lane has
+  // window entries in the vector, not once per element position that any lane
+  // has one.
+  constexpr int kEl = 16 / sizeof(TT);
   const bool far_mass = use_p && !use_k;
+  const bool windowed = g.lo > 0.0f;
   unsigned long long fm = 0, um = 0;
   uint32_t uc = 0;
-  float fv = 0.0f, uv = 0.0f;
-  adj_visit<TT, NT, false>(row, V, vec, pol, [&](float x) {
-    const float z = (M - x) * c;
-    const int b = adj_bin1(z, g);
-    if (b == -2) {
-      ++uc;
-      uv += ex2(-z);
-      return;
+  adj_visit_vec<TT, NT>(row, V, vec, pol, [&](const float* x, int n) {
+    uint32_t wm = 0;
+    float fv = 0.0f, uv = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kEl; ++e) {
+      if (e >= n) break;
+      const float z = (M - x[e]) * c;
+      const int b = adj_bin1(z, g);
+      if (b == -2) {
+        ++uc;
+        uv += ex2(-z);
+      } else if (b < 0) {
+        if (far_mass && z < 64.0f) fv += ex2(-z);  // NaN and z >= 64 add nothing
+      } else {
+        wm |= 1u << e;
+      }
     }
-    if (b < 0) {
-      if (far_mass && z < 64.0f) fv += ex2(-z);  // NaN and z >= 64 add nothing
-      return;
-    }
-    const uint32_t k = order_key(x);
-    atomicAdd(&A.cnt1[b], 1u);
-    atomicAdd(&A.mass1[b], adj_mass(z, fscale));
-    atomicMin(&A.kmin1[b], k);
-    atomicMax(&A.kmax1[b], k);
-  }, [&]() {
-    if (far_mass) {
-      fm += __float2ull_rn(fv * fscale);
-      fv = 0.0f;
-    }
-    if (g.lo > 0.0f) {
-      um += __float2ull_rn(uv * fscale);
-      uv = 0.0f;
+    if (far_mass) fm += __float2ull_rn(fv * fscale);
+    if (windowed) um += __float2ull_rn(uv * fscale);
+    while (wm) {
+      const int e = __ffs(wm) - 1;
+      wm &= wm - 1;
+      float xe = x[0];
+#pragma unroll
+      for (int k = 1; k < kEl; ++k) xe = (e == k) ? x[k] : xe;
+      const float z = (M - xe) * c;
+      const int b = adj_bin1(z, g);
+      const uint32_t k = order_key(xe);
+      atomicAdd(&A.cnt1[b], 1u);
+      atomicAdd(&A.mass1[b], adj_mass(z, fscale));
+      atomicMin(&A.kmin1[b], k);
+      atomicMax(&A.kmax1[b], k);
     }
   });
   __syncthreads();
   unsigned long long tm = fm + um;
   for (int j = tid; j < kAdjBins1; j += NT) tm += A.mass1[j];
   kept = adj_block_sum<NT>(tm, A);
-  const unsigned long long above_m = g.lo > 0.0f ? adj_block_sum<NT>(um, A) : 0ull;
-  const uint32_t above_c = g.lo > 0.0f ? (uint32_t)adj_block_sum<NT>(uc, A) : 0u;
+  const unsigned long long above_m = windowed ? adj_block_sum<NT>(um, A) : 0ull;
+  const uint32_t above_c = windowed ? (uint32_t)adj_block_sum<NT>(uc, A) : 0u;
   key = 0u;  // below every logit
   for (int pass = 0; pass < 2; ++pass) {
     const bool by_mass = pass == 1;
