@@ -87,6 +87,12 @@ def _load():
         lib.oracle_rejection_sample_adj.restype = i32
         lib.oracle_adjusted_probs.argtypes = [vp, i32, i32, dbl, i32, dbl, i32, vp, vp, vp]
         lib.oracle_adjusted_probs.restype = i32
+        lib.oracle_tree_verify_request.argtypes = [i64, i32, vp, i32, vp, vp, vp, i32, dbl, u64,
+                                                   vp, vp, vp, vp]
+        lib.oracle_tree_verify_request.restype = i32
+        lib.oracle_tree_verify.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, dbl, u64, vp, vp,
+                                           vp, vp]
+        lib.oracle_tree_verify.restype = i32
         _lib = lib
         return lib
 
@@ -245,3 +251,64 @@ def adjusted_probs(row: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0
     if st < 0:
         raise ValueError(f"oracle_adjusted_probs failed with status {st}")
     return (p, (int(lo[0]), int(hi[0]))) if with_range else p
+
+
+@dataclass
+class TreeResult:
+    tokens: np.ndarray          # int32 [N_nodes]; request b uses slots cu[b] .. cu[b+1]-1
+    num_accepted: np.ndarray    # int32 [B]
+    path: np.ndarray            # int32 [N_nodes]  accepted node indices (within the request), -1
+    near_tie: np.ndarray        # int32 [B]
+    status: int
+
+
+def tree_verify(target_logits: np.ndarray, draft_probs: np.ndarray | None, node_tokens,
+                node_parent, cu_num_nodes, T: float, seed: int,
+                dtype: str | None = None) -> TreeResult:
+    """A batch of token trees in the flattened layout (see ``specdec_oracle.c``,
+    oracle_tree_verify): request b owns nodes cu[b] .. cu[b+1]-1, node 0 of a
+    request being its context; parents are indices within the request."""
+    lib = _load()
+    logits, dt = _logits_array(target_logits, dtype)
+    cu = np.ascontiguousarray(cu_num_nodes, dtype=np.int32)
+    tok = np.ascontiguousarray(node_tokens, dtype=np.int32)
+    par = np.ascontiguousarray(node_parent, dtype=np.int32)
+    B = cu.shape[0] - 1
+    V = logits.shape[-1]
+    n = int(cu[-1])
+    if logits.reshape(-1, V).shape[0] != n or tok.shape[0] != n or par.shape[0] != n:
+        raise ValueError("one target row, token and parent per node")
+    q = None
+    if draft_probs is not None:
+        q = np.ascontiguousarray(draft_probs, dtype=np.float32)
+        if q.reshape(-1, V).shape[0] != n:
+            raise ValueError("one draft row per node")
+    tokens = np.empty(n, np.int32)
+    nacc = np.empty(B, np.int32)
+    path = np.empty(n, np.int32)
+    tie = np.empty(B, np.int32)
+    st = lib.oracle_tree_verify(_ptr(logits), dt, _ptr(q), _ptr(tok), _ptr(par), _ptr(cu), B, V,
+                                float(T), seed & 0xFFFFFFFFFFFFFFFF, _ptr(tokens), _ptr(nacc),
+                                _ptr(path), _ptr(tie))
+    return TreeResult(tokens, nacc, path, tie, int(st))
+
+
+def tree_verify_request(b: int, target_rows: np.ndarray, draft_rows: np.ndarray | None,
+                        node_tokens, node_parent, T: float, seed: int,
+                        dtype: str | None = None) -> TreeResult:
+    """One token tree with global request index ``b`` (the generator key)."""
+    lib = _load()
+    logits, dt = _logits_array(target_rows, dtype)
+    V = logits.shape[-1]
+    n = logits.reshape(-1, V).shape[0]
+    tok = np.ascontiguousarray(node_tokens, dtype=np.int32)
+    par = np.ascontiguousarray(node_parent, dtype=np.int32)
+    q = None if draft_rows is None else np.ascontiguousarray(draft_rows, dtype=np.float32)
+    tokens = np.empty(n, np.int32)
+    nacc = np.empty(1, np.int32)
+    path = np.empty(n, np.int32)
+    tie = np.empty(1, np.int32)
+    st = lib.oracle_tree_verify_request(b, n, _ptr(logits), dt, _ptr(q), _ptr(tok), _ptr(par), V,
+                                        float(T), seed & 0xFFFFFFFFFFFFFFFF, _ptr(tokens),
+                                        _ptr(nacc), _ptr(path), _ptr(tie))
+    return TreeResult(tokens, nacc, path, tie, int(st))

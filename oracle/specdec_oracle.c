@@ -591,3 +591,205 @@ int oracle_rejection_sample(const void* target_logits, int dtype, const float* d
                                      out_q_x, out_accept, out_pos_near_tie, out_near_tie, NULL,
                                      NULL);
 }
+
+/* ---------------------------------------------------------------------- */
+/* Token trees: several candidates per position                           */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * Verifies one request whose drafts form a tree (the tree drafts of EAGLE
+ * that the tarrragon page names among the drafter variants and the vllbc page
+ * places under the same accept rule, Section 3.6: any drafter works as long
+ * as its probabilities are known at verification).  The pages give no
+ * multi-candidate rule; the one taken here applies their single-candidate
+ * step again after each rejection, which the correctness argument of the
+ * vllbc page's Appendix A.1 (or Theorem 3.5's proof on the bloss0m page)
+ * covers at every round:
+ *   node 0 is the context the target has seen; every other node j carries a
+ *   draft token tok[j] and a parent par[j] < j; the children of a node, in
+ *   increasing index order, are candidates for the same next token, drawn
+ *   independently from that node's draft distribution q_u (draft row u);
+ *   target row u is the target's distribution p_u of the token after node u.
+ *   At node u with target t = p_u: for r = 0, 1, ... test child c_r:
+ *     accept when U(seed, b, u, 0, r) < min(1, t(x)/q_u(x)), x = tok[c_r]
+ *     (the same conventions as the chain for t(x) = 0 or q_u(x) = 0);
+ *     accepted: emit x and continue at node c_r;
+ *     rejected: t <- norm(max(0, t - q_u)) (t itself if that is zero
+ *     everywhere, the chain's zero-residual reading).
+ *   All children rejected, or a node without children: draw the extra token
+ *   from t with the exponential race, uniforms U(seed, b, u, 1, v), and stop.
+ * On a chain (node i + 1 the only child of node i, carrying draft i) this is
+ * exactly the chain verifier: same uniforms, same residual, same race.
+ * T == 0 is greedy: the first child whose token equals the target argmax of
+ * node u (lowest index on ties) is accepted; otherwise that argmax is the
+ * extra token.
+ *   tgt   [n_nodes, V] target rows, dtype; draft [n_nodes, V] (rows of nodes
+ *         with children are read; NULL at T == 0)
+ *   tok, par [n_nodes]: par[0] = -1 and 0 <= par[j] < j for j > 0
+ * Outputs (any may be NULL):
+ *   tokens [n_nodes]   accepted tokens, then the extra token, then -1
+ *   num_accepted [1]   accepted tokens (the depth reached)
+ *   path [n_nodes]     accepted node indices, then -1
+ *   near_tie [1]       an accept test within 1e-5 relative of its threshold, or
+ *                      a race whose two best keys are within 1e-5 relative
+ * Returns ORACLE_OK, ORACLE_BAD_DRAFT_ID (a token outside [0, V): treated as
+ * t(x) = q(x) = 0, rejected), ORACLE_INVALID_ARG (a malformed tree) or
+ * ORACLE_OOM.
+ */
+int oracle_tree_verify_request(int64_t b, int n_nodes, const void* tgt, int dtype,
+                               const float* draft, const int32_t* tok, const int32_t* par, int V,
+                               double T, uint64_t seed, int32_t* tokens, int32_t* num_accepted,
+                               int32_t* path, int32_t* near_tie) {
+  if (n_nodes <= 0 || V <= 0 || !tgt || !tok || !par) return ORACLE_INVALID_ARG;
+  if (par[0] != -1) return ORACLE_INVALID_ARG;
+  for (int j = 1; j < n_nodes; ++j)
+    if (par[j] < 0 || par[j] >= j) return ORACLE_INVALID_ARG;
+  if (T > 0.0 && !draft && n_nodes > 1) return ORACLE_INVALID_ARG;
+  int status = ORACLE_OK;
+  int tie = 0;
+  int depth = 0;
+  int t_extra = -1;
+  double* t = (double*)malloc(sizeof(double) * (size_t)V);
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  int* acc_path = (int*)malloc(sizeof(int) * (size_t)n_nodes);
+  int* emitted = (int*)malloc(sizeof(int) * (size_t)n_nodes);
+  if (!t || !w || !acc_path || !emitted) {
+    free(t);
+    free(w);
+    free(acc_path);
+    free(emitted);
+    return ORACLE_OOM;
+  }
+  int u = 0;
+  for (;;) {
+    if (T == 0.0) {
+      const int g = argmax_row(tgt, dtype, (size_t)u, V);
+      int next = -1;
+      for (int c = u + 1; c < n_nodes; ++c) {
+        if (par[c] != u) continue;
+        if (tok[c] < 0 || tok[c] >= V) status = ORACLE_BAD_DRAFT_ID;
+        if (tok[c] == g) {
+          next = c;
+          break;
+        }
+      }
+      if (next < 0) {
+        t_extra = g;
+        break;
+      }
+      acc_path[depth] = next;
+      emitted[depth++] = tok[next];
+      u = next;
+      continue;
+    }
+    softmax_row(tgt, dtype, (size_t)u, V, T, t);
+    const float* q = draft ? draft + (size_t)u * (size_t)V : NULL;
+    int next = -1, r = 0;
+    for (int c = u + 1; c < n_nodes && next < 0; ++c) {
+      if (par[c] != u) continue;
+      const int x = tok[c];
+      double px = 0.0, qx = 0.0;
+      if (x >= 0 && x < V) {
+        px = t[x];
+        qx = (double)q[x];
+      } else {
+        status = ORACLE_BAD_DRAFT_ID;
+      }
+      double ratio;
+      if (px == 0.0)
+        ratio = 0.0;
+      else if (qx == 0.0)
+        ratio = INFINITY;
+      else
+        ratio = px / qx;
+      const double a = ratio < 1.0 ? ratio : 1.0;
+      const double rr = oracle_uniform(seed, (uint64_t)b, (uint64_t)u, 0, (uint64_t)r);
+      const double hi = rr > a ? rr : a;
+      if (fabs(rr - a) <= NEAR_TIE_REL * hi) tie = 1;
+      if (rr < a) {
+        next = c;
+        break;
+      }
+      /* rejected: the target of the next candidate is the normalised residual */
+      double z = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double d = t[v] - (double)q[v];
+        w[v] = d > 0.0 ? d : 0.0;
+        z += w[v];
+      }
+      if (z > 0.0)
+        for (int v = 0; v < V; ++v) t[v] = w[v] / z;
+      ++r;
+    }
+    if (next >= 0) {
+      acc_path[depth] = next;
+      emitted[depth++] = tok[next];
+      u = next;
+      continue;
+    }
+    /* exponential race over t: argmax over t(v) > 0 of t(v) / E_v */
+    double k1 = -INFINITY, k2 = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+      if (!(t[v] > 0.0)) continue;
+      const double e = -log(oracle_uniform(seed, (uint64_t)b, (uint64_t)u, 1, (uint64_t)v));
+      const double key = t[v] / e;
+      if (key > k1) {
+        k2 = k1;
+        k1 = key;
+        t_extra = v;
+      } else if (key > k2) {
+        k2 = key;
+      }
+    }
+    if (k2 > -INFINITY && (k1 - k2) <= NEAR_TIE_REL * k1) tie = 1;
+    break;
+  }
+  if (tokens) {
+    for (int i = 0; i < depth; ++i) tokens[i] = emitted[i];
+    tokens[depth] = t_extra;
+    for (int i = depth + 1; i < n_nodes; ++i) tokens[i] = -1;
+  }
+  if (num_accepted) *num_accepted = depth;
+  if (path)
+    for (int i = 0; i < n_nodes; ++i) path[i] = i < depth ? acc_path[i] : -1;
+  if (near_tie) *near_tie = tie;
+  free(t);
+  free(w);
+  free(acc_path);
+  free(emitted);
+  return status;
+}
+
+/*
+ * A batch of trees in a flattened layout: request b owns nodes cu[b] ..
+ * cu[b+1]-1 (its node 0 first), with their target rows, draft rows, tokens and
+ * parents (parents are indices within the request).  Output slots follow the
+ * nodes.
+ */
+int oracle_tree_verify(const void* target_logits, int dtype, const float* draft_probs,
+                       const int32_t* node_tokens, const int32_t* node_parent, const int32_t* cu,
+                       int B, int V, double T, uint64_t seed, int32_t* out_tokens,
+                       int32_t* out_num_accepted, int32_t* out_path, int32_t* out_near_tie) {
+  if (B <= 0 || V <= 0 || !target_logits || !node_tokens || !node_parent || !cu)
+    return ORACLE_INVALID_ARG;
+  if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_UNSUPPORTED_DTYPE;
+  if (!(T >= 0.0) || isinf(T)) return ORACLE_INVALID_ARG;
+  if (cu[0] != 0) return ORACLE_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (cu[b + 1] <= cu[b]) return ORACLE_INVALID_ARG;
+  const size_t esize = dtype == ORACLE_DTYPE_F32 ? 4 : 2;
+  int status = ORACLE_OK;
+  for (int b = 0; b < B; ++b) {
+    const size_t n0 = (size_t)cu[b];
+    const int n = cu[b + 1] - cu[b];
+    const int s = oracle_tree_verify_request(
+        b, n, (const char*)target_logits + n0 * (size_t)V * esize, dtype,
+        (T > 0.0 && draft_probs) ? draft_probs + n0 * (size_t)V : NULL, node_tokens + n0,
+        node_parent + n0, V, T, seed, out_tokens ? out_tokens + n0 : NULL,
+        out_num_accepted ? out_num_accepted + b : NULL, out_path ? out_path + n0 : NULL,
+        out_near_tie ? out_near_tie + b : NULL);
+    if (s == ORACLE_OOM || s == ORACLE_INVALID_ARG) return s;
+    if (s != ORACLE_OK) status = s;
+  }
+  return status;
+}
