@@ -71,7 +71,13 @@ def parse_args(argv=None):
                          "'secondary' (default: the ragged workload 3 beside the plain large "
                          "workload 4; -1: none)")
     ap.add_argument("--secondary-steps", type=int, default=200)
+    ap.add_argument("--tree", action="store_true",
+                    help="token trees (specdec_tree_verify): B=256 requests of V=256000 bf16 "
+                         "target rows, f32 draft rows, T=1, every tree 4 root candidates, 2 "
+                         "below each, then chains (29 nodes)")
     args = ap.parse_args(argv)
+    if args.tree:
+        args.secondary = -1
     if args.secondary is None:
         plain = (args.config == 4 and args.batch is None and args.vocab is None
                  and args.draft == "probs" and args.path == "auto" and args.top_k is None
@@ -488,6 +494,96 @@ def measure(args, dist, dev, sd, config: int, steps: int, warmup: int) -> Measur
                     step=step)
 
 
+TREE_SHAPE = [4, 2, 1, 1]
+
+
+def measure_tree(args, dist, dev, sd):
+    """Times the token-tree entry point: the kernel walks every request from
+    its root, so the bytes it must read are the target rows of the nodes it
+    visits and the draft rows of those that have children (counted from the
+    accepted paths); reported against that."""
+    import torch
+    from speculative_decoding_rejection_decode_gb300.inputs import make_tree_workload
+    B = args.batch or 256
+    Vv = args.vocab or 256000
+    w = make_tree_workload(name=f"token trees B={B} V={Vv} bf16 T=1 shape {TREE_SHAPE}", B=B, V=Vv,
+                           dtype="bf16", T=1.0, seed=7, shape=TREE_SHAPE, device=dev)
+    v = sd.Verifier(dev)
+    out = None
+
+    def step():
+        nonlocal out
+        out = v.tree(w.target_logits, w.draft_probs, w.node_tokens, w.node_parent, w.cu, w.T,
+                     w.seed, request_offset=dist.rank * B, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if v.get_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    # rows the walk must read: every visited node's target row, and the draft
+    # row of each visited node that has children
+    nacc = out.num_accepted.cpu()
+    path = out.path.cpu()
+    cu = w.cu.cpu()
+    par = w.node_parent.cpu()
+    visited = int(nacc.sum()) + B
+    with_children = 0
+    for b in range(B):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        nodes = [0] + [int(x) for x in path[s0:s0 + int(nacc[b])]]
+        kids = set(int(x) for x in par[s0 + 1:s1])
+        with_children += sum(1 for u in nodes if u in kids)
+    alg = visited * Vv * 2 + with_children * Vv * 4
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.25)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    for k in range(K):
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clocks = sampler.stop()
+    if v.get_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = dist.max(ev[0][0].elapsed_time(ev[-1][1]) / 1e3)
+    ms = total_s * 1e3 / K
+    n_draft = w.n_nodes - B
+    peak, peak_kind = measured_peak_gbs()
+    achieved = alg / (statistics.mean(step_ms) / 1e3) / 1e9
+    in_bytes = w.n_nodes * Vv * 6
+    res = {
+        "metric": "verified draft nodes/s", "value": n_draft * dist.world * K / total_s,
+        "unit": "nodes/s", "n_gpus": dist.world, "steps": K, "warmup": max(3, args.warmup),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "V": Vv, "target_dtype": "bf16",
+                   "draft_dtype": "f32", "T": 1.0, "tree_shape": TREE_SHAPE,
+                   "nodes": w.n_nodes, "input_bytes": in_bytes,
+                   "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush"},
+        "requests_per_s": B * dist.world * K / total_s,
+        "accepted_per_request": float(nacc.double().mean()),
+        "roofline": {"bound": "hbm", "kernel": "tree_walk_kernel", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": alg,
+                     "algorithmic_bytes_rule": "target row of every visited node + draft row "
+                                               "of every visited node with children",
+                     "avg_launch_ms": statistics.mean(step_ms)},
+        "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
+        "gpu_launches": K, "clocks": clocks,
+    }
+    v.close()
+    return res
+
+
 def main():
     args = parse_args()
     dist = Dist()
@@ -504,6 +600,12 @@ def main():
 
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
+    if args.tree:
+        res = measure_tree(args, dist, dev, sd)
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+        dist.close()
+        return
     # the second workload the roofline target names (the ragged batch), timed in
     # the same run and reported beside the headline as "secondary"
     secondary = None

@@ -87,6 +87,7 @@ typedef struct specdec_ctx* specdec_handle_t;
 #define SPECDEC_DEVERR_BAD_CU 2u
 #define SPECDEC_DEVERR_CAPACITY 4u
 #define SPECDEC_DEVERR_TIMEOUT 8u
+#define SPECDEC_DEVERR_BAD_TREE 16u   /* specdec_tree_verify: a node's parent is not an earlier node */
 
 /* execution paths (specdec_set_path); AUTO picks per call */
 #define SPECDEC_PATH_AUTO 0
@@ -188,6 +189,55 @@ int specdec_rejection_sample_topk_topp(
     const int32_t* top_k, const float* top_p, uint64_t seed, uint64_t request_offset,
     int32_t* out_tokens, int32_t* out_num_accepted, float* out_beta, float* out_target_prob,
     float* out_draft_prob, int32_t* out_accept, void* stream);
+
+/* ---- token trees: several candidates per position --------------------------
+ * Verifies B requests whose drafts form trees (the tree drafts of EAGLE that the
+ * tarrragon page lists among the drafter variants; the vllbc page, Section 3.6,
+ * notes that any drafter works as long as its probabilities are known at
+ * verification).  The pages state the accept rule for one candidate per
+ * position; this entry point applies it again after each rejection, with the
+ * normalised residual as the next candidate's target (the correctness argument
+ * of the vllbc page's Appendix A.1 holds at every round):
+ *   request b owns nodes cu[b] .. cu[b+1]-1 (at least one); its node 0 is the
+ *   context the target has seen, every other node j carries a draft token
+ *   node_tokens[j] and a parent node_parent[j] (an index within the request,
+ *   < j; node 0 has -1).  The children of a node, in node order, are
+ *   candidates for the same next token, each drawn independently from that
+ *   node's draft distribution q_u.  Target row j (target_logits, [N, V], N =
+ *   cu[B]) is the target's distribution after node j, draft row j
+ *   (draft_probs, [N, V] float32) the drafter's; draft rows of nodes without
+ *   children are never read.
+ *   At node u with target t (first p_u = softmax(target row u / T)), child r
+ *   with token x is accepted when U(seed, b, u, 0, r) < min(1, t(x) / q_u(x));
+ *   otherwise t <- norm(max(0, t - q_u)) (t unchanged if that is zero
+ *   everywhere).  An accepted child becomes the next node; after the last
+ *   rejection, or at a node without children, the extra token is drawn from t
+ *   by the exponential race with U(seed, b, u, 1, v).  On a chain (node i + 1
+ *   the only child of node i) this is exactly specdec_rejection_sample_ex.
+ *   T == 0 is greedy: the first child whose token is the argmax of target row
+ *   u (lowest index on ties) is accepted; otherwise that argmax is the extra
+ *   token; draft_probs may be NULL.
+ * Outputs (device; slots follow the nodes):
+ *   out_tokens        [N] int32: request b's accepted tokens in slots
+ *                     cu[b] .. cu[b] + n_b - 1, the extra token in slot
+ *                     cu[b] + n_b, later slots -1
+ *   out_num_accepted  [B] int32 n_b (the depth reached)
+ *   out_path          [N] int32 or NULL: the accepted nodes (indices within the
+ *                     request) in the first n_b slots of the request, then -1
+ * request_offset as in specdec_rejection_sample_ex.  Host-checked errors as for
+ * the other entry points (draft_probs NULL at T > 0 is SPECDEC_ERR_INVALID_ARG).
+ * Device-detected: a token outside [0, V) is a rejected candidate
+ * (SPECDEC_DEVERR_BAD_DRAFT_ID); a request whose tree is malformed writes
+ * nothing (SPECDEC_DEVERR_BAD_TREE; SPECDEC_DEVERR_BAD_CU for cu[0] != 0 or a
+ * request without nodes); a node with more than 256 children has only its
+ * first 256 tested (SPECDEC_DEVERR_CAPACITY).  One CTA walks a request: per
+ * visited node one pass over its target row, one over the row pair for every
+ * rejection followed by another candidate, and one for the race. */
+int specdec_tree_verify(specdec_handle_t h, const void* target_logits, int dtype,
+                        const float* draft_probs, const int32_t* node_tokens,
+                        const int32_t* node_parent, const int32_t* cu_num_nodes, int B, int V,
+                        float T, uint64_t seed, uint64_t request_offset, int32_t* out_tokens,
+                        int32_t* out_num_accepted, int32_t* out_path, void* stream);
 
 /* Reads the handle's sticky device error word (SPECDEC_DEVERR_* bits) into
  * *device_error and clears it.  Queues the read on `stream` and waits for it, so

@@ -23,7 +23,8 @@ _LAZY = {"Verifier", "VerifyOutput", "SpecdecError", "uniform", "neg_log_uniform
          "specdec_set_adjust_counters", "specdec_last_path", "specdec_uniform",
          "specdec_neg_log_uniform", "specdec_selection_mass", "selection_mass",
          "specdec_status_string", "specdec_destroy",
-         "specdec_rejection_sample_noalloc", "SPECDEC_F32", "SPECDEC_BF16",
+         "specdec_rejection_sample_noalloc", "specdec_tree_verify", "TreeOutput",
+         "SPECDEC_F32", "SPECDEC_BF16",
          "SPECDEC_PATH_AUTO", "SPECDEC_PATH_FUSED", "SPECDEC_PATH_TWO_PASS", "SPECDEC_PATH_SWEEP",
          "SPECDEC_PATH_STREAM", "SPECDEC_PATH_PAIR", "SPECDEC_PATH_DUAL", "SPECDEC_PATH_GREEDY"}
 

@@ -28,6 +28,7 @@ SPECDEC_DEVERR_BAD_DRAFT_ID = 1
 SPECDEC_DEVERR_BAD_CU = 2
 SPECDEC_DEVERR_CAPACITY = 4
 SPECDEC_DEVERR_TIMEOUT = 8
+SPECDEC_DEVERR_BAD_TREE = 16
 
 SPECDEC_NOALLOC_MAX_ROWS = 16384
 SPECDEC_NOALLOC_MAX_BATCH = 4096
@@ -77,6 +78,8 @@ _neg_log = _fn("specdec_neg_log_uniform", _i32, _u32, _i64, _vp, _vp)
 _sel_mass = _fn("specdec_selection_mass", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
 _rs_noalloc = _fn("specdec_rejection_sample_noalloc", _i32, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
                   _f32, _u64, _i64, _vp, _vp, _vp, _vp, _vp)
+_tree = _fn("specdec_tree_verify", _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _f32,
+            _u64, _u64, _vp, _vp, _vp, _vp)
 _status_string = _fn("specdec_status_string", ctypes.c_char_p, _i32)
 _destroy = _fn("specdec_destroy", _i32, _vp)
 
@@ -160,6 +163,14 @@ def specdec_rejection_sample_noalloc(target_logits, dtype, draft_probs, draft_id
                        out_beta, out_device_error, stream)
 
 
+def specdec_tree_verify(h, target_logits, dtype, draft_probs, node_tokens, node_parent,
+                        cu_num_nodes, B, V, T, seed, request_offset, out_tokens, out_num_accepted,
+                        out_path, stream) -> int:
+    return _tree(h, target_logits, dtype, draft_probs, node_tokens, node_parent, cu_num_nodes, B,
+                 V, T, seed & 0xFFFFFFFFFFFFFFFF, request_offset, out_tokens, out_num_accepted,
+                 out_path, stream)
+
+
 def specdec_status_string(status: int) -> str:
     return _status_string(status).decode()
 
@@ -173,4 +184,5 @@ EXPORTED = ["specdec_create", "specdec_reserve", "specdec_rejection_sample",
             "specdec_get_error", "specdec_set_path",
             "specdec_set_timing_events", "specdec_set_adjust_counters",
             "specdec_last_path", "specdec_uniform", "specdec_neg_log_uniform",
-            "specdec_selection_mass", "specdec_rejection_sample_noalloc", "specdec_status_string", "specdec_destroy"]
+            "specdec_selection_mass", "specdec_rejection_sample_noalloc", "specdec_tree_verify",
+            "specdec_status_string", "specdec_destroy"]

@@ -9,6 +9,7 @@
 #include <new>
 
 #include "kernels.cuh"
+#include "tree.cuh"
 
 using namespace specdec;
 
@@ -48,7 +49,8 @@ struct specdec_ctx {
   int smem_optin = 0;
   Workspace ws;
   uint32_t* small = nullptr;  // [0] sticky error word, [1] deferred-request count,
-                              // [2..3] sweep-kernel work counter (64-bit)
+                              // [2..3] sweep-kernel work counter (64-bit),
+                              // [4..5] tree-walk request counter (64-bit)
   bool reserved = false;
   int64_t res_rows = 0;
   int res_b = 0;
@@ -505,6 +507,47 @@ int specdec_rejection_sample(specdec_handle_t h, const void* target_logits, int 
   return specdec_rejection_sample_ex(h, target_logits, dtype, draft_probs, draft_ids,
                                      cu_num_draft_tokens, B, V, T, seed, 0, out_tokens,
                                      out_num_accepted, out_beta, nullptr, nullptr, nullptr, stream);
+}
+
+int specdec_tree_verify(specdec_handle_t h, const void* target_logits, int dtype,
+                        const float* draft_probs, const int32_t* node_tokens,
+                        const int32_t* node_parent, const int32_t* cu_num_nodes, int B, int V,
+                        float T, uint64_t seed, uint64_t request_offset, int32_t* out_tokens,
+                        int32_t* out_num_accepted, int32_t* out_path, void* stream) {
+  if (!h) return SPECDEC_ERR_INVALID_ARG;
+  if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED_DTYPE;
+  if (B <= 0 || V <= 0 || V > (1 << 30)) return SPECDEC_ERR_INVALID_ARG;
+  if (!std::isfinite(T) || T < 0.0f) return SPECDEC_ERR_INVALID_ARG;
+  if (!target_logits || !node_tokens || !node_parent || !cu_num_nodes || !out_tokens ||
+      !out_num_accepted || (T > 0.0f && !draft_probs))
+    return SPECDEC_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return SPECDEC_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TreeArgs a = {};
+  a.logits = target_logits;
+  a.q = T > 0.0f ? draft_probs : nullptr;
+  a.tok = node_tokens;
+  a.par = node_parent;
+  a.cu = cu_num_nodes;
+  a.B = B;
+  a.V = V;
+  a.c = T > 0.0f ? kLog2e / T : 0.0f;
+  a.seed = seed;
+  a.req_offset = request_offset;
+  a.out_tokens = out_tokens;
+  a.out_nacc = out_num_accepted;
+  a.out_path = out_path;
+  a.err = h->small;
+  a.counter = reinterpret_cast<unsigned long long*>(h->small + 4);
+  const int esize = dtype == SPECDEC_BF16 ? 2 : 4;
+  a.vec_ok = ((int64_t)V * esize) % 16 == 0 && ((int64_t)V * 4) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
+  if (h->ev_before) cudaEventRecord(h->ev_before, st);
+  const int rc = launch_tree(a, dtype, h->num_sms, st);
+  if (h->ev_after) cudaEventRecord(h->ev_after, st);
+  return rc;
 }
 
 int specdec_get_error(specdec_handle_t h, int* device_error, void* stream) {

@@ -200,3 +200,91 @@ def make_top_k_top_p(B: int, V: int, seed: int, top_k: int | None = None,
     k = torch.where((kind == 0) | (kind == 2) | (kind == 3), k, torch.zeros_like(k))
     p = torch.where((kind == 1) | (kind == 2) | (kind == 3), p, torch.ones_like(p))
     return k.to(device), p.to(device)
+
+
+# ----------------------------------------------------------------------------
+# Token trees (several candidates per position)
+# ----------------------------------------------------------------------------
+
+@dataclass
+class TreeWorkload:
+    name: str
+    B: int
+    V: int
+    dtype: str
+    T: float
+    seed: int
+    target_logits: torch.Tensor     # [N, V]: the target's row after every node
+    draft_probs: torch.Tensor | None  # [N, V] float32: the drafter's row at every node
+    node_tokens: torch.Tensor       # [N] int32 (node 0 of a request: 0)
+    node_parent: torch.Tensor       # [N] int32, within the request (node 0: -1)
+    cu: torch.Tensor                # [B+1] int32 node offsets
+
+    @property
+    def n_nodes(self) -> int:
+        return int(self.cu[-1])
+
+    def to(self, device) -> "TreeWorkload":
+        mv = lambda t: None if t is None else t.to(device)
+        return TreeWorkload(self.name, self.B, self.V, self.dtype, self.T, self.seed,
+                            mv(self.target_logits), mv(self.draft_probs), mv(self.node_tokens),
+                            mv(self.node_parent), mv(self.cu))
+
+
+def tree_shape(branching) -> list[int]:
+    """Parents of a full tree whose level d nodes have branching[d] children
+    each, in breadth-first order (node 0 the root)."""
+    par = [-1]
+    level = [0]
+    for k in branching:
+        nxt = []
+        for u in level:
+            for _ in range(k):
+                par.append(u)
+                nxt.append(len(par) - 1)
+        level = nxt
+    return par
+
+
+def make_tree_workload(*, name: str, B: int, V: int, dtype: str, T: float, seed: int,
+                       shape="random", max_nodes: int = 16, target_std: float = 3.0,
+                       noise_std: float = 1.0, device="cpu") -> TreeWorkload:
+    """Synthetic token trees.  ``shape`` is "random" (each request gets 1 ..
+    max_nodes nodes, every node's parent drawn uniformly from the earlier
+    nodes) or a list of per-level branching factors (the same full tree for
+    every request).  Target rows ~ N(0, target_std^2) (bf16 or f32); the
+    drafter's row at node u is softmax((L_u + N(0, noise_std^2)) / T) of that
+    node's own target row (T = 1 for greedy); the token of node j is drawn
+    from the drafter's row at its parent, independently for every child, as the
+    candidates of a tree drafter are."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    pars = []
+    for b in range(B):
+        if shape == "random":
+            n = int(torch.randint(1, max_nodes + 1, (1,), generator=g))
+            par = [-1] + [int(torch.randint(0, j, (1,), generator=g)) for j in range(1, n)]
+        else:
+            par = tree_shape(shape)
+        pars.append(par)
+    sizes = torch.tensor([len(p) for p in pars], dtype=torch.int64)
+    cu = torch.zeros(B + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(sizes, 0)
+    N = int(cu[-1])
+    dev = torch.device(device)
+    gd = torch.Generator(device=dev)
+    gd.manual_seed(seed + 1)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    logits = (torch.randn(N, V, generator=gd, device=dev) * target_std).to(tdt)
+    dT = float(T) if T > 0 else 1.0
+    q = torch.softmax((logits.float() + torch.randn(N, V, generator=gd, device=dev) * noise_std)
+                      / dT, dim=-1)
+    parent = torch.tensor([p for par in pars for p in par], dtype=torch.int32)
+    base = torch.repeat_interleave(cu[:-1], sizes)
+    gpar = (base + parent.to(torch.int64).clamp(min=0)).to(dev)
+    tokens = torch.multinomial(q[gpar], 1, generator=gd).squeeze(1).to(torch.int32)
+    root = (parent == -1).to(dev)
+    tokens = torch.where(root, torch.zeros_like(tokens), tokens)
+    return TreeWorkload(name=name, B=B, V=V, dtype=dtype, T=float(T), seed=seed,
+                        target_logits=logits, draft_probs=q if T > 0 else None,
+                        node_tokens=tokens, node_parent=parent.to(dev), cu=cu.to(torch.int32).to(dev))

@@ -16,7 +16,7 @@ from ._lib import (SPECDEC_BF16, SPECDEC_F32, SPECDEC_PATH_AUTO, SPECDEC_PATH_DU
                    specdec_rejection_sample_noalloc, specdec_rejection_sample_topk_topp,
                    specdec_reserve, specdec_set_adjust_counters,
                    specdec_set_path, specdec_set_timing_events, specdec_status_string,
-                   specdec_uniform)
+                   specdec_tree_verify, specdec_uniform)
 
 
 class SpecdecError(RuntimeError):
@@ -107,6 +107,16 @@ class Verifier:
         _check(rc, "specdec_get_error")
         return e
 
+    def tree(self, target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
+             node_tokens: torch.Tensor, node_parent: torch.Tensor, cu_num_nodes: torch.Tensor,
+             T: float, seed: int, *, request_offset: int = 0, with_path: bool = True,
+             out: "TreeOutput | None" = None) -> "TreeOutput":
+        """Verifies token trees (several candidates per position) on the current
+        torch stream: specdec_tree_verify.  One target and one draft row per
+        node; node_parent holds indices within each request (node 0: -1)."""
+        return _tree_call(self, target_logits, draft_probs, node_tokens, node_parent,
+                          cu_num_nodes, T, seed, request_offset, with_path, out)
+
     def __call__(self, target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                  draft_ids: torch.Tensor, cu_num_draft_tokens: torch.Tensor, T: float, seed: int,
                  *, with_beta: bool = True, extended: bool = False,
@@ -171,6 +181,47 @@ class Verifier:
                 _ptr(out.num_accepted), _ptr(out.beta), stream)
         _check(rc, "specdec_rejection_sample")
         return out
+
+
+@dataclass
+class TreeOutput:
+    tokens: torch.Tensor         # int32 [N] request b: slots cu[b] .. cu[b+1]-1
+    num_accepted: torch.Tensor   # int32 [B]
+    path: torch.Tensor | None    # int32 [N] accepted nodes (indices within the request), -1
+
+
+def _tree_call(v: "Verifier", target_logits, draft_probs, node_tokens, node_parent, cu_num_nodes,
+               T, seed, request_offset=0, with_path=True, out: TreeOutput | None = None):
+    for t in (target_logits, node_tokens, node_parent, cu_num_nodes):
+        if t.device != v.device or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous tensors on the verifier's device")
+    if draft_probs is not None and (draft_probs.device != v.device
+                                    or draft_probs.dtype != torch.float32
+                                    or not draft_probs.is_contiguous()):
+        raise ValueError("draft_probs must be a contiguous float32 tensor on the device")
+    if target_logits.dtype == torch.float32:
+        dtype = SPECDEC_F32
+    elif target_logits.dtype == torch.bfloat16:
+        dtype = SPECDEC_BF16
+    else:
+        raise TypeError("target_logits must be float32 or bfloat16")
+    for t in (node_tokens, node_parent, cu_num_nodes):
+        if t.dtype != torch.int32:
+            raise TypeError("node_tokens, node_parent and cu_num_nodes must be int32")
+    B = cu_num_nodes.numel() - 1
+    N = node_tokens.numel()
+    V = target_logits.shape[-1]
+    if out is None:
+        out = TreeOutput(tokens=torch.empty(N, dtype=torch.int32, device=v.device),
+                         num_accepted=torch.empty(B, dtype=torch.int32, device=v.device),
+                         path=torch.empty(N, dtype=torch.int32, device=v.device)
+                         if with_path else None)
+    rc = specdec_tree_verify(v.handle, _ptr(target_logits), dtype, _ptr(draft_probs),
+                             _ptr(node_tokens), _ptr(node_parent), _ptr(cu_num_nodes), B, V,
+                             float(T), int(seed), int(request_offset), _ptr(out.tokens),
+                             _ptr(out.num_accepted), _ptr(out.path), _stream_handle(v.device))
+    _check(rc, "specdec_tree_verify")
+    return out
 
 
 def uniform(seed: int, b: int, pos: int, stream_id: int, v0: int, n: int,

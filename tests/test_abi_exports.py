@@ -67,6 +67,8 @@ def test_host_checked_errors_return_before_any_device_work(lib):
     assert _lib.specdec_rejection_sample_topk_topp(None, 1, 0, 1, 1, 1, 1, 8, 1.0, None, None, 0,
                                                    0, 1, 1, None, None, None, None,
                                                    None) == INVALID
+    assert _lib.specdec_tree_verify(None, 1, 0, 1, 1, 1, 1, 1, 8, 1.0, 0, 0, 1, 1, None,
+                                    None) == INVALID
     # generator, log and mass diagnostics: bad sizes refused, empty requests are no-ops
     assert _lib.specdec_uniform(0, 0, 0, 0, 0, -1, None, None) == INVALID
     assert _lib.specdec_uniform(0, 0, 0, 0, 0, 0, None, None) == 0
