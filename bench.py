@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="threads of the all-cores oracle rate (0: every usable core; 1: skip it)")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-compare", action="store_true",
+                    help="also time e2e with the pinned inputs placed by default (no CPU pinning)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--secondary", type=int, default=None,
@@ -648,6 +650,11 @@ def main():
     }
     if not args.no_e2e:
         result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp)
+        if args.e2e_compare:
+            d = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp,
+                            local=False)
+            result["e2e_default_placement"] = {k: d[k] for k in ("value", "ms_per_step",
+                                                                 "h2d_gbps", "host_placement")}
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         rate, nreq, npos, el = oracle_sample_rate(w, args.cpu_seconds, top_k=tk, top_p=tp)
         cpu = host_cpu_model()
@@ -673,11 +680,57 @@ def main():
     dist.close()
 
 
-def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None):
+def parse_cpu_list(text: str) -> set[int]:
+    """'0-3,8,10-11' -> {0, 1, 2, 3, 8, 10, 11}."""
+    cpus = set()
+    for part in text.split(","):
+        part = part.strip()
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_local_cpus(index: int, topo: str | None = None):
+    """The host CPUs nvidia-smi reports as local to GPU `index` ('CPU Affinity'
+    of `nvidia-smi topo -m`) and its NUMA node, or (None, None)."""
+    try:
+        if topo is None:
+            topo = subprocess.run(["nvidia-smi", "topo", "-m"], capture_output=True, text=True,
+                                  timeout=30).stdout
+        lines = [ln for ln in topo.splitlines() if ln.strip()]
+        head = next(ln for ln in lines if "CPU Affinity" in ln)
+        cols = [c.strip() for c in head.split("\t")]
+        row = next(ln for ln in lines if ln.split("\t")[0].strip() == f"GPU{index}")
+        cells = [c.strip() for c in row.split("\t")]
+        cpus = parse_cpu_list(cells[cols.index("CPU Affinity")])
+        numa = cells[cols.index("NUMA Affinity")] if "NUMA Affinity" in cols else None
+        usable = cpus & os.sched_getaffinity(0)
+        return (usable or None), numa
+    except (OSError, StopIteration, ValueError, IndexError, subprocess.SubprocessError):
+        return None, None
+
+
+def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None, local=True):
     """Same metric through the public API with the step's inputs in pinned host
     memory: every step copies them to the device, verifies, and reads the
-    tokens, counts and beta back."""
+    tokens, counts and beta back.  With `local`, the process runs on the CPUs
+    local to the GPU while the pinned buffers are allocated and filled, so
+    that their pages sit in the GPU's own NUMA node (a GB300 reaches its own
+    Grace's memory over the chip-to-chip link)."""
     import torch
+    placement = "default (the process's CPUs)"
+    old_aff = os.sched_getaffinity(0)
+    if local:
+        cpus, numa = gpu_local_cpus(dev.index if dev.index is not None else 0)
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+            placement = (f"CPUs local to the GPU ({len(cpus)} of {len(old_aff)}; NUMA node "
+                         f"{numa}) while the pinned buffers were allocated and filled")
     host = {}
     for name in ("target_logits", "draft_probs", "draft_ids", "cu"):
         t = getattr(w, name)
@@ -716,9 +769,11 @@ def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     total_s = dist.max(e0.elapsed_time(e1) / 1e3)
+    os.sched_setaffinity(0, old_aff)
     return {"value": w.n_draft * dist.world * steps / total_s, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": total_s * 1e3 / steps}
+            "ms_per_step": total_s * 1e3 / steps, "host_placement": placement,
+            "h2d_gbps": h2d / (total_s / steps) / 1e9}
 
 
 def run_reference(args, dist):

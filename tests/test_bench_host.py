@@ -140,3 +140,16 @@ def test_reference_arm_two_ranks_rank0_prints_once():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_gpu_local_cpus_from_topology_table():
+    topo = ("\tGPU0\tGPU1\tNIC0\tCPU Affinity\tNUMA Affinity\tGPU NUMA ID\n"
+            "GPU0\t X \tNV18\tSYS\t0-1,3\t0\t2\n"
+            "GPU1\tNV18\t X \tSYS\t100000-100003\t1\t10\n")
+    cpus, numa = bench.gpu_local_cpus(0, topo)
+    usable = os.sched_getaffinity(0)
+    assert cpus == ({0, 1, 3} & usable or None) and numa == "0"
+    assert bench.gpu_local_cpus(1, topo) == (None, "1")      # none of those CPUs exist here
+    assert bench.gpu_local_cpus(2, topo) == (None, None)
+    assert bench.gpu_local_cpus(0, "garbage") == (None, None)
+    assert bench.parse_cpu_list("0-3,8,10-11") == {0, 1, 2, 3, 8, 10, 11}
