@@ -268,6 +268,21 @@ int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after
  * NULL stops. */
 int specdec_set_adjust_counters(specdec_handle_t h, uint64_t* device_counters);
 
+/* Test hook for the bounded waits (no counterpart in the pages; it exercises
+ * this library's failure handling without faulting the GPU).  The kernels that
+ * wait on another CTA (the cluster paths) give every wait a time limit and, when
+ * it runs out, set SPECDEC_DEVERR_TIMEOUT and leave.  With
+ * mode = SPECDEC_FAULT_PAIR_STALL, later calls on the pair path (forced with
+ * specdec_set_path) have rank 0 of every 2-CTA cluster withhold the first work
+ * slot from rank 1, whose wait then runs out after wait_limit_ns (1 ns .. 2 s;
+ * the pair kernel's waits all use this limit while the hook is on); the call's
+ * outputs are then undefined and the error word carries the timeout bit.
+ * SPECDEC_FAULT_NONE (wait_limit_ns ignored) restores normal operation.
+ * Returns SPECDEC_OK or SPECDEC_ERR_INVALID_ARG. */
+#define SPECDEC_FAULT_NONE 0
+#define SPECDEC_FAULT_PAIR_STALL 1
+int specdec_set_fault_injection(specdec_handle_t h, int mode, uint64_t wait_limit_ns);
+
 /* Path the last call on this handle used (SPECDEC_PATH_FUSED, _TWO_PASS, _SWEEP,
  * _STREAM, _PAIR, _DUAL or _GREEDY), and the cluster size of a cluster path (0
  * otherwise). */

@@ -30,6 +30,9 @@ SPECDEC_DEVERR_CAPACITY = 4
 SPECDEC_DEVERR_TIMEOUT = 8
 SPECDEC_DEVERR_BAD_TREE = 16
 
+SPECDEC_FAULT_NONE = 0
+SPECDEC_FAULT_PAIR_STALL = 1
+
 SPECDEC_NOALLOC_MAX_ROWS = 16384
 SPECDEC_NOALLOC_MAX_BATCH = 4096
 
@@ -73,6 +76,7 @@ _set_path = _fn("specdec_set_path", _i32, _vp, _i32)
 _set_events = _fn("specdec_set_timing_events", _i32, _vp, _vp, _vp)
 _last_path = _fn("specdec_last_path", _i32, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
 _set_adj_ctr = _fn("specdec_set_adjust_counters", _i32, _vp, _vp)
+_set_fault = _fn("specdec_set_fault_injection", _i32, _vp, _i32, _u64)
 _uniform = _fn("specdec_uniform", _i32, _u64, _u64, _u64, _u32, _u64, _i64, _vp, _vp)
 _neg_log = _fn("specdec_neg_log_uniform", _i32, _u32, _i64, _vp, _vp)
 _sel_mass = _fn("specdec_selection_mass", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
@@ -124,6 +128,10 @@ def specdec_set_timing_events(h: int, before_rows, after_rows) -> int:
 
 def specdec_set_adjust_counters(h: int, device_counters) -> int:
     return _set_adj_ctr(h, device_counters)
+
+
+def specdec_set_fault_injection(h: int, mode: int, wait_limit_ns: int) -> int:
+    return _set_fault(h, mode, wait_limit_ns)
 
 
 def specdec_get_error(h: int, stream) -> tuple[int, int]:
@@ -183,6 +191,7 @@ EXPORTED = ["specdec_create", "specdec_reserve", "specdec_rejection_sample",
             "specdec_rejection_sample_ex", "specdec_rejection_sample_topk_topp",
             "specdec_get_error", "specdec_set_path",
             "specdec_set_timing_events", "specdec_set_adjust_counters",
+            "specdec_set_fault_injection",
             "specdec_last_path", "specdec_uniform", "specdec_neg_log_uniform",
             "specdec_selection_mass", "specdec_rejection_sample_noalloc", "specdec_tree_verify",
             "specdec_status_string", "specdec_destroy"]

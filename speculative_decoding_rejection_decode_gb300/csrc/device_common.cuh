@@ -325,12 +325,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_acq_cluster(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -86,6 +86,11 @@ struct Params {
   int tbuf_bytes;          // bytes of the target slice buffer (rank 0, 128-aligned)
   int nq;                  // draft ring stages
   int vec_ok;              // rows are 16-byte aligned: vector loads allowed
+  // test hook (specdec_set_fault_injection): the pair kernel's bounded waits
+  // give up after wait_ns (0: the default 2 s), and with stall_peer its rank 0
+  // withholds the first work slot from rank 1, whose wait then runs out
+  uint64_t wait_ns;
+  int stall_peer;
 };
 
 constexpr int kChunk = 4096;          // elements per bulk copy / pipeline step
@@ -1742,6 +1747,7 @@ __global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
   const int nunits = vec ? V / kEl : V;
   const int half = (nunits + 1) / 2;
   const int lo = rank ? half : 0, hi = rank ? nunits : half;
+  const uint64_t limit = P.wait_ns ? P.wait_ns : kWaitLimitNs;
   bool ok = true;
 
   for (uint32_t k = 0;; ++k) {
@@ -1771,12 +1777,13 @@ __global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
       }
       const uint32_t slot = smem_addr(&S.desc[par]);
       for (uint32_t r = 0; r < 2; ++r) {
+        if (P.stall_peer && r == 1 && k == 0) continue;  // test hook: rank 1 is left waiting
         st_cluster_v4(mapa(slot, r), __int_as_float((int)(u & 0xFFFFFFFF)),
                       __int_as_float((int)(u >> 32)), __int_as_float(prefix), 0.f);
         mbar_arrive_cluster(mapa(smem_addr(&S.bdesc[par]), r));
       }
     }
-    if (tid == 0) S.flag = (ok && mbar_wait_cluster(smem_addr(&S.bdesc[par]), ph)) ? 0 : 1;
+    if (tid == 0) S.flag = (ok && mbar_wait_cluster(smem_addr(&S.bdesc[par]), ph, limit)) ? 0 : 1;
     __syncthreads();
     if (S.flag) {
       ok = false;
@@ -1822,7 +1829,7 @@ __global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
         st_cluster_v4(mapa(slot, r), mh, sh, __int_as_float(pfx), 0.f);
         mbar_arrive_cluster(mapa(smem_addr(&S.bms[par]), r));
       }
-      ok = mbar_wait_cluster(smem_addr(&S.bms[par]), ph);
+      ok = mbar_wait_cluster(smem_addr(&S.bms[par]), ph, limit);
       float M = -INFINITY, Ssum = 0.0f;
       softmax_merge(M, Ssum, S.ms[par][0].x, S.ms[par][0].y, P.c);
       softmax_merge(M, Ssum, S.ms[par][1].x, S.ms[par][1].y, P.c);
@@ -1881,7 +1888,7 @@ __global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
       st_cluster_v4(mapa(smem_addr(&S.part[par][rank]), 0), bh, rh.w, rh.e, __int_as_float(rh.idx));
       mbar_arrive_cluster(mapa(smem_addr(&S.bred[par]), 0));
       if (rank == 0) {
-        ok = mbar_wait_cluster(smem_addr(&S.bred[par]), ph);
+        ok = mbar_wait_cluster(smem_addr(&S.bred[par]), ph, limit);
         float bt = 0.0f;
         Race tb = race_none();
         for (int r = 0; r < 2; ++r) {

@@ -66,6 +66,8 @@ struct specdec_ctx {
   int occ_cache[2][5][2] = {};  // [dtype][cluster index] -> {smem, clusters}
   int adj_smem_set[2] = {0, 0};  // dynamic shared memory set on the adjusted sweep kernel
   unsigned long long* adj_ctr = nullptr;  // caller's selection counters (profiling), or null
+  int fault_mode = 0;           // specdec_set_fault_injection
+  uint64_t fault_wait_ns = 0;
 };
 
 namespace {
@@ -465,6 +467,8 @@ int specdec_rejection_sample_topk_topp(
              reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
              reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
   P.sched = reinterpret_cast<unsigned long long*>(h->small + 2);
+  P.wait_ns = h->fault_wait_ns;
+  P.stall_peer = h->fault_mode == SPECDEC_FAULT_PAIR_STALL ? 1 : 0;
   // AUTO: with fewer requests than sweep CTAs (2 per SM), the sweep kernel's
   // later rows of a request usually decide before its earlier rows finish and
   // their races go to the race kernel; the pair kernel holds half as many rows
@@ -581,6 +585,16 @@ int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after
 int specdec_set_adjust_counters(specdec_handle_t h, uint64_t* device_counters) {
   if (!h) return SPECDEC_ERR_INVALID_ARG;
   h->adj_ctr = reinterpret_cast<unsigned long long*>(device_counters);
+  return SPECDEC_OK;
+}
+
+int specdec_set_fault_injection(specdec_handle_t h, int mode, uint64_t wait_limit_ns) {
+  if (!h || (mode != SPECDEC_FAULT_NONE && mode != SPECDEC_FAULT_PAIR_STALL))
+    return SPECDEC_ERR_INVALID_ARG;
+  if (mode != SPECDEC_FAULT_NONE && (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull))
+    return SPECDEC_ERR_INVALID_ARG;
+  h->fault_mode = mode;
+  h->fault_wait_ns = mode == SPECDEC_FAULT_NONE ? 0 : wait_limit_ns;
   return SPECDEC_OK;
 }
 

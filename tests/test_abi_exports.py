@@ -59,6 +59,7 @@ def test_host_checked_errors_return_before_any_device_work(lib):
     assert _lib.specdec_set_path(None, 0) == INVALID
     assert _lib.specdec_set_timing_events(None, None, None) == INVALID
     assert _lib.specdec_set_adjust_counters(None, None) == INVALID
+    assert _lib.specdec_set_fault_injection(None, 0, 0) == INVALID
     assert _lib.specdec_last_path(None)[0] == INVALID
     assert _lib.specdec_get_error(None, None)[0] == INVALID
     assert _lib.specdec_destroy(None) == INVALID
