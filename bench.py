@@ -63,7 +63,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="threads of the all-cores oracle rate (0: every usable core; 1: skip it)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-streams", type=int, default=1,
+                    help="host-to-device copies of a step split over this many streams")
     ap.add_argument("--e2e-compare", action="store_true",
                     help="also time e2e with the pinned inputs placed by default (no CPU pinning)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -74,7 +76,7 @@ def parse_args(argv=None):
                          "workload 4; -1: none)")
     ap.add_argument("--secondary-steps", type=int, default=200)
     ap.add_argument("--tree", action="store_true",
-                    help="token trees (specdec_tree_verify): B=256 requests of V=256000 bf16 "
+                    help="token trees (specdec_tree_verify): B=512 requests of V=256000 bf16 "
                          "target rows, f32 draft rows, T=1, every tree 4 root candidates, 2 "
                          "below each, then chains (29 nodes)")
     args = ap.parse_args(argv)
@@ -506,7 +508,7 @@ def measure_tree(args, dist, dev, sd):
     accepted paths); reported against that."""
     import torch
     from speculative_decoding_rejection_decode_gb300.inputs import make_tree_workload
-    B = args.batch or 256
+    B = args.batch or 512
     Vv = args.vocab or 256000
     w = make_tree_workload(name=f"token trees B={B} V={Vv} bf16 T=1 shape {TREE_SHAPE}", B=B, V=Vv,
                            dtype="bf16", T=1.0, seed=7, shape=TREE_SHAPE, device=dev)
@@ -649,10 +651,11 @@ def main():
         "alpha_mean_beta": float(out.beta.double().mean()),
     }
     if not args.no_e2e:
-        result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp)
+        result["e2e"] = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp,
+                                    copy_streams=args.e2e_streams)
         if args.e2e_compare:
             d = measure_e2e(v, w, out, dev, stream, args.e2e_steps, dist, offset, tk, tp,
-                            local=False)
+                            local=False, copy_streams=args.e2e_streams)
             result["e2e_default_placement"] = {k: d[k] for k in ("value", "ms_per_step",
                                                                  "h2d_gbps", "host_placement")}
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -715,7 +718,8 @@ def gpu_local_cpus(index: int, topo: str | None = None):
         return None, None
 
 
-def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None, local=True):
+def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None, local=True,
+                copy_streams=1):
     """Same metric through the public API with the step's inputs in pinned host
     memory: every step copies them to the device, verifies, and reads the
     tokens, counts and beta back.  With `local`, the process runs on the CPUs
@@ -749,13 +753,46 @@ def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None, l
     h2d += sum(h.numel() * h.element_size() for _, h in adj.values())
     d2h = sum(h.numel() * h.element_size() for h in h_out.values())
 
+    # the step's host-to-device copies in `copy_streams` pieces on as many
+    # streams (each piece waits for the previous step's verify, the verify
+    # waits for every piece)
+    nstreams = max(1, int(copy_streams))
+    cstreams = [torch.cuda.Stream(dev) for _ in range(nstreams)] if nstreams > 1 else []
+    free_ev = torch.cuda.Event()
+    free_ev.record(stream)
+
     def one():
-        for name, h in host.items():
-            getattr(w, name).copy_(h, non_blocking=True)
-        for d, h in adj.values():
-            d.copy_(h, non_blocking=True)
+        if cstreams:
+            done = []
+            pieces = []
+            for name, h in host.items():
+                d = getattr(w, name)
+                rows = d.shape[0] if d.dim() else 1
+                step_rows = max(1, (rows + nstreams - 1) // nstreams) if d.dim() else rows
+                for r0 in range(0, rows, step_rows):
+                    pieces.append((d[r0:r0 + step_rows] if d.dim() else d,
+                                   h[r0:r0 + step_rows] if d.dim() else h))
+            for d, h in adj.values():
+                pieces.append((d, h))
+            for i, (d, h) in enumerate(pieces):
+                cs = cstreams[i % nstreams]
+                cs.wait_event(free_ev)
+                with torch.cuda.stream(cs):
+                    d.copy_(h, non_blocking=True)
+            for cs in cstreams:
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                done.append(ev)
+            for ev in done:
+                stream.wait_event(ev)
+        else:
+            for name, h in host.items():
+                getattr(w, name).copy_(h, non_blocking=True)
+            for d, h in adj.values():
+                d.copy_(h, non_blocking=True)
         v(w.target_logits, w.draft_probs, w.draft_ids, w.cu, w.T, w.seed, out=out,
           request_offset=offset, top_k=tk, top_p=tp)
+        free_ev.record(stream)
         for k, h in h_out.items():
             h.copy_(getattr(out, k), non_blocking=True)
 
@@ -773,7 +810,7 @@ def measure_e2e(v, w, out, dev, stream, steps, dist, offset, tk=None, tp=None, l
     return {"value": w.n_draft * dist.world * steps / total_s, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": total_s * 1e3 / steps, "host_placement": placement,
-            "h2d_gbps": h2d / (total_s / steps) / 1e9}
+            "h2d_gbps": h2d / (total_s / steps) / 1e9, "copy_streams": max(1, int(copy_streams))}
 
 
 def run_reference(args, dist):

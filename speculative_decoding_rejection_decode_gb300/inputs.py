@@ -248,7 +248,7 @@ def tree_shape(branching) -> list[int]:
 
 def make_tree_workload(*, name: str, B: int, V: int, dtype: str, T: float, seed: int,
                        shape="random", max_nodes: int = 16, target_std: float = 3.0,
-                       noise_std: float = 1.0, device="cpu") -> TreeWorkload:
+                       noise_std: float = 1.0, device="cpu", chunk_rows: int = 512) -> TreeWorkload:
     """Synthetic token trees.  ``shape`` is "random" (each request gets 1 ..
     max_nodes nodes, every node's parent drawn uniformly from the earlier
     nodes) or a list of per-level branching factors (the same full tree for
@@ -275,10 +275,14 @@ def make_tree_workload(*, name: str, B: int, V: int, dtype: str, T: float, seed:
     gd = torch.Generator(device=dev)
     gd.manual_seed(seed + 1)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    logits = (torch.randn(N, V, generator=gd, device=dev) * target_std).to(tdt)
+    logits = torch.empty(N, V, dtype=tdt, device=dev)
+    q = torch.empty(N, V, dtype=torch.float32, device=dev)
     dT = float(T) if T > 0 else 1.0
-    q = torch.softmax((logits.float() + torch.randn(N, V, generator=gd, device=dev) * noise_std)
-                      / dT, dim=-1)
+    for r0 in range(0, N, chunk_rows):          # in row blocks: no full-size temporaries
+        r1 = min(N, r0 + chunk_rows)
+        logits[r0:r1] = (torch.randn(r1 - r0, V, generator=gd, device=dev) * target_std).to(tdt)
+        noisy = logits[r0:r1].float() + torch.randn(r1 - r0, V, generator=gd, device=dev) * noise_std
+        q[r0:r1] = torch.softmax(noisy / dT, dim=-1)
     parent = torch.tensor([p for par in pars for p in par], dtype=torch.int32)
     base = torch.repeat_interleave(cu[:-1], sizes)
     gpar = (base + parent.to(torch.int64).clamp(min=0)).to(dev)
