@@ -640,7 +640,8 @@ def main():
         c = ctr.cpu().tolist()
         result["adjust_selection_per_step"] = {
             "adjusted_rows": c[0], "sample_edge_in_tail": c[1], "edge_past_cut": c[2],
-            "key_refinement_passes": c[3], "rows_without_threshold": c[4]}
+            "key_refinement_passes": c[3], "rows_without_threshold": c[4],
+            "resolved_on_value_bins": c[5]}
     nacc = out.num_accepted.double()
     result["acceptance"] = {
         # accepted drafts / proposed drafts (the timinsight guide's definition)

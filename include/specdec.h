@@ -264,7 +264,8 @@ int specdec_set_timing_events(specdec_handle_t h, void* before_rows, void* after
  * caller, zeroed by the caller): [0] adjusted rows, [1] rows whose sampled
  * estimate put the edge in the tail, [2] rows whose edge lay past the
  * estimated cut (both take a selection over the whole row), [3] key-refinement
- * passes, [4] rows left without a threshold (NaN logits), [5..7] unused.
+ * passes, [4] rows left without a threshold (NaN logits), [5] rows resolved on
+ * bins of one bf16 value each (one counting pass), [6..7] unused.
  * NULL stops. */
 int specdec_set_adjust_counters(specdec_handle_t h, uint64_t* device_counters);
 

@@ -513,6 +513,35 @@ __device__ __forceinline__ void softmax_acc16(const uint4& w, float& m, float& s
   }
 }
 
+// As softmax_acc16, with the sum kept as an unevaluated pair s + l: each
+// vector's partial sum is added by Knuth's TwoSum, whose rounding error goes
+// to l, so the row's sum does not lose the low bits of its many additions.
+template <typename TT>
+__device__ __forceinline__ void softmax_acc16_ff(const uint4& w, float& m, float& s, float& l,
+                                                 float c) {
+  constexpr int kEl = 16 / sizeof(TT);
+  float x[kEl];
+  unpack16<TT>(w, x);
+  float vm = x[0];
+#pragma unroll
+  for (int k = 1; k < kEl; ++k) vm = fmaxf(vm, x[k]);
+  if (vm > m) {
+    const float f = ex2((m - vm) * c);
+    s *= f;
+    l *= f;
+    m = vm;
+  }
+  if (m != -INFINITY) {
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kEl; ++k) a += ex2((x[k] - m) * c);
+    const float t = s + a;
+    const float bp = t - s;
+    l += (s - (t - bp)) + (a - bp);
+    s = t;
+  }
+}
+
 // Sweep-2 work on 4 consecutive vocabulary entries starting at v.  With kMask
 // the entries below tau are outside the adjusted row (p = 0).
 template <bool kHasQ, bool kRace, bool kMask>
@@ -733,6 +762,62 @@ __device__ __forceinline__ void sweep1(const TT* row, int lo, int hi, bool vec, 
   s = s0;
 }
 
+// Sweep 1 of the adjusted kernel: as sweep1, with the per-thread sum carried
+// as s + l (softmax_acc16_ff); the two accumulators are merged with the
+// products' and the addition's rounding errors moved to l.
+template <typename TT, int NT>
+__device__ __forceinline__ void sweep1_ff(const TT* row, int hi, bool vec, float c, uint64_t pol,
+                                          float& m, float& s, float& l) {
+  float m0 = -INFINITY, s0 = 0.0f, l0 = 0.0f, m1 = -INFINITY, s1 = 0.0f, l1 = 0.0f;
+  const int tid = threadIdx.x;
+  if (vec) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    int j = tid;
+    for (; j + 7 * NT < hi; j += 8 * NT) {
+      uint4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = ldg_hint(rv + j + u * NT, pol);
+#pragma unroll
+      for (int u = 0; u < 8; u += 2) {
+        softmax_acc16_ff<TT>(a[u], m0, s0, l0, c);
+        softmax_acc16_ff<TT>(a[u + 1], m1, s1, l1, c);
+      }
+    }
+    for (; j < hi; j += NT) softmax_acc16_ff<TT>(ldg_hint(rv + j, pol), m0, s0, l0, c);
+  } else {
+    for (int v = tid; v < hi; v += NT) {
+      const float xv = load_logit(row + v);
+      if (xv > m0) {
+        const float f = ex2((m0 - xv) * c);
+        s0 *= f;
+        l0 *= f;
+        m0 = xv;
+      }
+      if (m0 != -INFINITY) {
+        const float a = ex2((xv - m0) * c);
+        const float t = s0 + a;
+        const float bp = t - s0;
+        l0 += (s0 - (t - bp)) + (a - bp);
+        s0 = t;
+      }
+    }
+  }
+  const float mn = fmaxf(m0, m1);
+  if (mn == -INFINITY) {
+    m = mn;
+    s = 0.0f;
+    l = 0.0f;
+    return;
+  }
+  const float f0 = ex2((m0 - mn) * c), f1 = ex2((m1 - mn) * c);
+  const float a = s0 * f0, b = s1 * f1;
+  const float t = a + b;
+  const float bp = t - a;
+  m = mn;
+  s = t;
+  l = (l0 * f0 + l1 * f1) + ((a - (t - bp)) + (b - bp)) + (fmaf(s0, f0, -a) + fmaf(s1, f1, -b));
+}
+
 // ---------------------------------------------------------------------------
 // Top-k / top-p adjusted target rows (the vllbc page's Section 2.2 note: top-k
 // and top-p fold into the adjusted p before the same rejection test).
@@ -756,6 +841,13 @@ __device__ __forceinline__ void sweep1(const TT* row, int lo, int hi, bool vec, 
 //      left.
 // When the edge lies beyond Zc (or in a row holding -inf or NaN at the edge)
 // step 2 runs again with 64 bins per unit and a last bin that takes the rest.
+// bf16 rows whose entries above the cut take at most 2048 values (the common
+// case: the values between the cut and the max span a few octaves of 128
+// bf16 values each) replace steps 2 and 3 by one pass with a bin per value:
+// one 32-bit count per entry, the bin's mass its count times the value's mass
+// (adj_run_keys); the top-p bound without top-k then takes the row's whole
+// mass from sweep 1, summed with error compensation and added up as integers
+// of the same scale.
 // Counts are exact; masses are integers (pow2_neg(z) scaled by 2^F with
 // V 2^F <= 2^62), so the shared-memory histograms add up the same way in any
 // order, the result does not depend on thread timing, and the top-p test
@@ -768,8 +860,11 @@ constexpr int kAdjMaxKeyLevels = 4;  // 1024^4 > 2^32: key levels always end on 
 
 // Selection statistics (specdec_set_adjust_counters): adjusted rows, rows whose
 // sample put the edge in the last bin, rows whose edge lay past the cut,
-// key-refinement passes, rows left without a threshold.
-enum AdjCounter { kAdjRows = 0, kAdjTail, kAdjMiss, kAdjKeyPass, kAdjNone, kAdjCounters = 8 };
+// key-refinement passes, rows left without a threshold, rows resolved on
+// bins of one bf16 value each.
+enum AdjCounter {
+  kAdjRows = 0, kAdjTail, kAdjMiss, kAdjKeyPass, kAdjNone, kAdjExact, kAdjCounters = 8
+};
 __device__ __forceinline__ void adj_count(unsigned long long* ctr, int i) {
   if (ctr && threadIdx.x == 0) atomicAdd(ctr + i, 1ull);
 }
@@ -831,6 +926,12 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 }
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// 16-bit order key of a bf16 value held as a float (the upper half of its
+// order key: distinct bf16 values get distinct, ordered keys), and back.
+__device__ __forceinline__ uint32_t key16(float x) { return order_key(x) >> 16; }
+__device__ __forceinline__ float key16_value(uint32_t k) {
+  return key_value((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu));
 }
 
 // Level-1 geometry: bins of width 1/scale in z (scale a power of two).  With
@@ -1180,6 +1281,64 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
   return true;
 }
 
+// bf16 rows whose entries at or above x_lo take at most 2048 values
+// (key16(M) - key16(x_lo) < 2048): one pass counts the entries of each value in
+// bin j = key16(M) - key16(x) (bin 0 holds the max).  A bin holds one value, so
+// its mass is its count times that value's integer mass (the sum of the
+// per-entry masses), no key refinement follows, and an entry costs one 32-bit
+// shared-memory atomic.  Entries below x_lo (and NaN) are not counted: the top-k
+// edge needs only the counts above it, and the top-p bound is P times the
+// top-k set's mass, or, without top-k, P times s_all, the row's whole mass on
+// the same integer scale.  False when an edge lies below x_lo.
+template <int NT>
+__device__ bool adj_run_keys(const __nv_bfloat16* row, int V, bool vec, float M, float c,
+                             float fscale, int top_k, float top_p, bool use_k, bool use_p,
+                             unsigned long long s_all, float x_lo, uint64_t pol, AdjShared& A,
+                             uint32_t& key, unsigned long long& kept, uint32_t& kept_cnt) {
+  const int tid = threadIdx.x;
+  const uint32_t ktop = key16(M);
+  for (int j = tid; j < kAdjBins1; j += NT) A.cnt1[j] = 0u;
+  __syncthreads();
+  adj_visit_vec<__nv_bfloat16, NT>(row, V, vec, pol, [&](const float* x, int n) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e < n && x[e] >= x_lo) {
+        // x <= M, and x >= x_lo bounds the key from below: j < 2048 (guard only)
+        const uint32_t j = ktop - key16(x[e]);
+        atomicAdd(&A.cnt1[j < (uint32_t)kAdjBins1 ? j : kAdjBins1 - 1], 1u);
+      }
+    }
+  });
+  __syncthreads();
+  for (int j = tid; j < kAdjBins1; j += NT) {
+    const uint32_t n = A.cnt1[j];
+    A.mass1[j] =
+        n ? (unsigned long long)n * adj_mass((M - key16_value(ktop - j)) * c, fscale) : 0ull;
+  }
+  __syncthreads();
+  int j = kAdjBins1;
+  uint32_t kc = 0u;
+  unsigned long long km = 0ull;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool by_mass = pass == 1;
+    if (by_mass ? !use_p : !use_k) continue;
+    const double base = use_k ? (double)km : (double)s_all;
+    const double bound = by_mass ? (top_p > 0.0f ? (double)top_p : 0.0) * base : 0.0;
+    adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, by_mass, (uint32_t)top_k, bound, 0ull, A);
+    j = A.sel;
+    if (j < kAdjBins1) {
+      kc = A.ex_cnt + A.cnt1[j];
+      km = A.ex_mass + A.mass1[j];
+    }
+    __syncthreads();
+    if (j >= kAdjBins1) return false;
+  }
+  key = order_key(key16_value(ktop - j));
+  kept = km;
+  kept_cnt = kc;
+  return true;
+}
+
 // The cut for the level-1 histogram from a sample of the row: the z (64 bins
 // per unit) by which the sample passes 1.5 times its share of the top-k count,
 // or, for top-p alone, where the sample's tail beyond z (16 times its mass)
@@ -1253,10 +1412,12 @@ __device__ bool adj_estimate(const TT* row, int V, bool vec, float M, float c, f
 // Block-wide (every thread of the block calls it with the same arguments).
 // Returns false, leaving tau, S and kept_cnt alone, when no threshold exists
 // (NaN rows).
+// (mt, st + lt): this thread's sweep-1 max and compensated sum.
 template <typename TT, int NT>
 __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M, float c, int top_k,
-                           float top_p, bool use_k, bool use_p, uint64_t pol, AdjShared& A,
-                           float& tau, float& S, uint32_t& kept_cnt, unsigned long long* ctr) {
+                           float top_p, bool use_k, bool use_p, float mt, float st, float lt,
+                           uint64_t pol, AdjShared& A, float& tau, float& S, uint32_t& kept_cnt,
+                           unsigned long long* ctr) {
   // masses are pow2_neg(z) * 2^F with V * 2^F <= 2^62
   const int F = adj_mass_shift(V);
   const float fscale = adj_mass_scale(F);
@@ -1267,8 +1428,31 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
   bool ok = false;
   adj_count(ctr, kAdjRows);
   if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g, gw)) {
+    if constexpr (sizeof(TT) == 2) {
+      // bins of one value each, down to the window's cut (or the cut grid's)
+      const float x_lo = M - (gw.lo > 0.0f ? gw.cut : g.cut) / c;
+      if (key16(M) - key16(x_lo) < (uint32_t)kAdjBins1) {
+        unsigned long long s_all = 0ull;
+        bool fin = true;
+        if (use_p && !use_k) {
+          // the row's whole mass: every thread's compensated sum rescaled to
+          // the row max, as an integer of the masses' scale (exact to add)
+          const float f = ex2((mt - M) * c);
+          const float a = st * f;
+          const float r = lt * f + fmaf(st, f, -a);
+          fin = !__syncthreads_or(!(a == a) || !(r == r));  // NaN logits: the general path
+          const long long part = fin ? __float2ll_rn(a * fscale) + __float2ll_rn(r * fscale) : 0ll;
+          s_all = adj_block_sum<NT>((unsigned long long)part, A);
+        }
+        if (fin) {
+          ok = adj_run_keys<NT>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
+                                top_k, top_p, use_k, use_p, s_all, x_lo, pol, A, key, kept, kc);
+          if (ok) adj_count(ctr, kAdjExact);
+        }
+      }
+    }
     // the window grid first (when the sample gave one), then the cut grid
-    if (gw.lo > 0.0f)
+    if (!ok && gw.lo > 0.0f)
       ok = adj_run<TT, NT>(row, V, vec, M, c, fscale, top_k, top_p, use_k, use_p, gw, pol, A, key,
                            kept, kc, ctr);
     if (!ok)
@@ -1386,8 +1570,12 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
 
     // ---- sweep 1: (max, sum) ------------------------------------------------
     const int hi = vec ? V / kEl : V;
-    float m0, s0;
-    sweep1<TT, NT>(row, 0, hi, vec, P.c, keep, m0, s0);
+    float m0, s0, l0 = 0.0f;
+    if constexpr (kAdj)
+      sweep1_ff<TT, NT>(row, hi, vec, P.c, keep, m0, s0, l0);
+    else
+      sweep1<TT, NT>(row, 0, hi, vec, P.c, keep, m0, s0);
+    const float mt = m0, st = s0;  // this thread's own (max, sum), for adjusted rows
     warp_softmax(m0, s0, P.c);
     if (lane == 0) red[par][warp] = make_float4(m0, s0, 0.f, 0.f);
     __syncthreads();
@@ -1400,7 +1588,7 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
       const float pp = P.topp ? __ldg(P.topp + b) : 1.0f;
       const bool use_k = kk >= 1 && kk < V, use_p = !(pp >= 1.0f);
       if ((use_k || use_p) && M > -INFINITY && M < INFINITY)
-        adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, keep,
+        adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, mt, st, l0, keep,
                            *reinterpret_cast<AdjShared*>(adj_smem), tau, S, kept_cnt, P.adj_ctr);
     }
     // few kept entries: at most 1/8 of the 16-byte vectors hold one, so sweep 2

@@ -37,13 +37,11 @@ namespace specdec {
 
 namespace {
 
-constexpr int kTreeThreads = 512;
-constexpr int kTreeWarps = kTreeThreads / 32;
 
 // Sum over the row pair of w(v) = max(0, p(v) - C q(v)) (w = p without q),
 // p(v) = 2^((l_v - M) c) / S, and, with kRace, the race over w with key rkey.
 // Per-thread partial sum and race candidate (reduced by the caller).
-template <typename TT, bool kHasQ, bool kRace>
+template <typename TT, int NT, bool kHasQ, bool kRace>
 __device__ __forceinline__ void tree_pass(const TT* row, const float* qrow, int V, bool vec,
                                           float M, float c, float invS, float C, uint64_t rkey,
                                           uint64_t pol, float& wsum, Race& best) {
@@ -66,7 +64,7 @@ __device__ __forceinline__ void tree_pass(const TT* row, const float* qrow, int 
     const uint4* rv = reinterpret_cast<const uint4*>(row);
     const uint4* qv = reinterpret_cast<const uint4*>(qrow);
     const int nv = V / kEl;
-    for (int j = tid; j < nv; j += kTreeThreads) {
+    for (int j = tid; j < nv; j += NT) {
       float x[kEl];
       unpack16<TT>(ldg_hint(rv + j, pol), x);
 #pragma unroll
@@ -80,7 +78,7 @@ __device__ __forceinline__ void tree_pass(const TT* row, const float* qrow, int 
       }
     }
   } else {
-    for (int v = tid; v < V; v += kTreeThreads) {
+    for (int v = tid; v < V; v += NT) {
       const float p = ex2((load_logit(row + v) - M) * c) * invS;
       const float w = kHasQ ? fmaxf(p - C * __ldg(qrow + v), 0.0f) : p;
       wsum += w;
@@ -90,6 +88,7 @@ __device__ __forceinline__ void tree_pass(const TT* row, const float* qrow, int 
 }
 
 // Block-wide sum and race merge (every thread gets both); ends on a barrier.
+template <int NT>
 __device__ __forceinline__ void tree_reduce(float& wsum, Race& best, float4* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   wsum = warp_sum(wsum);
@@ -99,7 +98,7 @@ __device__ __forceinline__ void tree_reduce(float& wsum, Race& best, float4* red
   __syncthreads();
   float s = 0.0f;
   Race r = race_none();
-  for (int w = 0; w < kTreeWarps; ++w) {
+  for (int w = 0; w < (NT / 32); ++w) {
     s += red[w].x;
     race_merge(r, red[w].y, red[w].z, __float_as_int(red[w].w));
   }
@@ -107,8 +106,9 @@ __device__ __forceinline__ void tree_reduce(float& wsum, Race& best, float4* red
   best = r;
 }
 
-template <typename TT>
-__global__ void __launch_bounds__(kTreeThreads, 2) tree_walk_kernel(const TreeArgs P) {
+template <typename TT, int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) tree_walk_kernel(const TreeArgs P) {
+  constexpr int kTreeThreads = NT, kTreeWarps = NT / 32;
   __shared__ float4 red[kTreeWarps];
   __shared__ unsigned long long s_key[kTreeWarps];
   __shared__ int s_cnt[kTreeWarps];
@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_walk_kernel(const TreeAr
             // the residual the next candidate is tested against
             float W = 0.0f;
             Race none = race_none();
-            tree_pass<TT, true, false>(row, qrow, V, vec, M, P.c, invS, C + D, 0ull, drop, W, none);
-            tree_reduce(W, none, red);
+            tree_pass<TT, NT, true, false>(row, qrow, V, vec, M, P.c, invS, C + D, 0ull, drop, W, none);
+            tree_reduce<NT>(W, none, red);
             if (W > 0.0f) {
               C += D;
               D = W;
@@ -273,20 +273,20 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_walk_kernel(const TreeAr
           float W = 0.0f;
           Race best = race_none();
           if (K == 0) {
-            tree_pass<TT, false, true>(row, qrow, V, vec, M, P.c, invS, 0.0f, rkey, drop, W, best);
-            tree_reduce(W, best, red);
+            tree_pass<TT, NT, false, true>(row, qrow, V, vec, M, P.c, invS, 0.0f, rkey, drop, W, best);
+            tree_reduce<NT>(W, best, red);
           } else {
-            tree_pass<TT, true, true>(row, qrow, V, vec, M, P.c, invS, C + D, rkey, drop, W, best);
-            tree_reduce(W, best, red);
+            tree_pass<TT, NT, true, true>(row, qrow, V, vec, M, P.c, invS, C + D, rkey, drop, W, best);
+            tree_reduce<NT>(W, best, red);
             if (!(W > 0.0f)) {  // zero residual: the target stays the previous one
               W = 0.0f;
               best = race_none();
               if (C > 0.0f)
-                tree_pass<TT, true, true>(row, qrow, V, vec, M, P.c, invS, C, rkey, drop, W, best);
+                tree_pass<TT, NT, true, true>(row, qrow, V, vec, M, P.c, invS, C, rkey, drop, W, best);
               else
-                tree_pass<TT, false, true>(row, qrow, V, vec, M, P.c, invS, 0.0f, rkey, drop, W,
+                tree_pass<TT, NT, false, true>(row, qrow, V, vec, M, P.c, invS, 0.0f, rkey, drop, W,
                                            best);
-              tree_reduce(W, best, red);
+              tree_reduce<NT>(W, best, red);
             }
           }
           extra = best.w > 0.0f ? best.idx : 0;
@@ -320,11 +320,12 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_walk_kernel(const TreeAr
 int launch_tree(const TreeArgs& a, int dtype, int num_sms, cudaStream_t st) {
   if (cudaMemsetAsync(a.counter, 0, sizeof(unsigned long long), st) != cudaSuccess)
     return SPECDEC_ERR_CUDA;
-  const int grid = num_sms * 2;
+  constexpr int kThreads = 512, kPerSm = 2;
+  const int grid = num_sms * kPerSm;
   if (dtype == SPECDEC_BF16)
-    tree_walk_kernel<__nv_bfloat16><<<grid, kTreeThreads, 0, st>>>(a);
+    tree_walk_kernel<__nv_bfloat16, kThreads, kPerSm><<<grid, kThreads, 0, st>>>(a);
   else
-    tree_walk_kernel<float><<<grid, kTreeThreads, 0, st>>>(a);
+    tree_walk_kernel<float, kThreads, kPerSm><<<grid, kThreads, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
