@@ -726,6 +726,32 @@ __device__ __forceinline__ void sweep2(const TT* row, const float* qrow, int lo,
   }
 }
 
+// Sweep 2 of an adjusted row whose kept entries are all in its candidate list
+// (index and value of every entry at or above the counting pass's bound): beta
+// and the race over the listed entries at or above tau, with the same per-entry
+// arithmetic as sweep2 (every other entry has p' = 0: nothing to beta, no race
+// candidate; the race's winner does not depend on the order of the offers).
+template <int NT, bool kHasQ, bool kRace>
+__device__ __forceinline__ void sweep2_list(const uint2* cand, int n, const float* qrow, float M,
+                                            float c, float invS, float tau, bool resid,
+                                            uint64_t rkey, float& beta, Race& best, int excl) {
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint2 e = cand[i];
+    const float x = __uint_as_float(e.y);
+    if (!(x >= tau)) continue;
+    const float p = ex2((x - M) * c) * invS;
+    float q = 0.0f;
+    if constexpr (kHasQ) {
+      q = __ldg(qrow + e.x);
+      beta += fminf(p, q);
+    }
+    if constexpr (kRace) {
+      const float w = (kHasQ && resid) ? fmaxf(p - q, 0.0f) : ((int)e.x == excl ? 0.0f : p);
+      race_offer(best, w, rkey, e.x);
+    }
+  }
+}
+
 // Sweep 1 over vectors [lo, hi) (elements when not aligned): per-thread online
 // (max, sum) in two interleaved accumulators, merged on return.
 template <typename TT, int NT>
@@ -857,6 +883,7 @@ constexpr int kAdjBins1 = 2048;
 constexpr int kAdjBins2 = 1024;
 constexpr int kAdjSample = 16;       // the estimate reads one vector (or element) in 16
 constexpr int kAdjMaxKeyLevels = 4;  // 1024^4 > 2^32: key levels always end on one value
+constexpr int kAdjCand = 2048;       // candidate list of a top-k row (index, value)
 
 // Selection statistics (specdec_set_adjust_counters): adjusted rows, rows whose
 // sample put the edge in the last bin, rows whose edge lay past the cut,
@@ -883,6 +910,8 @@ struct AdjShared {
   int sel;
   uint32_t ex_cnt;
   unsigned long long ex_mass;
+  uint2 cand[kAdjCand];  // (index, logit bits) of the entries a counting pass saw
+  int ncand;
 };
 
 // Mass of an entry for the selection: 2^-z on a float32 definition that a CPU
@@ -1001,8 +1030,8 @@ __device__ __forceinline__ void adj_visit(const TT* row, int V, bool vec, uint64
   }
 }
 
-// Visits every entry of the row through f(x, n), a vector at a time: n = kEl
-// values of one 16-byte vector, or n = 1 on unaligned rows.
+// Visits every entry of the row through f(x, n, v), a vector at a time: n = kEl
+// values of one 16-byte vector, or n = 1 on unaligned rows; v = the index of x[0].
 template <typename TT, int NT, typename Fn>
 __device__ __forceinline__ void adj_visit_vec(const TT* row, int V, bool vec, uint64_t pol, Fn&& f) {
   constexpr int kEl = 16 / sizeof(TT);
@@ -1020,7 +1049,7 @@ __device__ __forceinline__ void adj_visit_vec(const TT* row, int V, bool vec, ui
         if (jn < nv) nxt = ldg_hint(rv + jn, pol);
         float x[kEl];
         unpack16<TT>(cur, x);
-        f(x, kEl);
+        f(x, kEl, j * kEl);
         if (jn >= nv) break;
         cur = nxt;
         j = jn;
@@ -1030,7 +1059,7 @@ __device__ __forceinline__ void adj_visit_vec(const TT* row, int V, bool vec, ui
     for (int v = tid; v < V; v += NT) {
       float x[kEl];
       x[0] = load_logit(row + v);
-      f(x, 1);
+      f(x, 1, v);
     }
   }
 }
@@ -1210,7 +1239,7 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
   const bool windowed = g.lo > 0.0f;
   unsigned long long fm = 0, um = 0;
   uint32_t uc = 0;
-  adj_visit_vec<TT, NT>(row, V, vec, pol, [&](const float* x, int n) {
+  adj_visit_vec<TT, NT>(row, V, vec, pol, [&](const float* x, int n, int) {
     uint32_t wm = 0;
     float fv = 0.0f, uv = 0.0f;
 #pragma unroll
@@ -1290,26 +1319,36 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
 // edge needs only the counts above it, and the top-p bound is P times the
 // top-k set's mass, or, without top-k, P times s_all, the row's whole mass on
 // the same integer scale.  False when an edge lies below x_lo.
+// With record, the counted entries' indices and values also go to A.cand;
+// ncand is then their number (every entry at or above x_lo, so every kept
+// one), or -1 when they did not fit (and always -1 without record).
 template <int NT>
 __device__ bool adj_run_keys(const __nv_bfloat16* row, int V, bool vec, float M, float c,
                              float fscale, int top_k, float top_p, bool use_k, bool use_p,
-                             unsigned long long s_all, float x_lo, uint64_t pol, AdjShared& A,
-                             uint32_t& key, unsigned long long& kept, uint32_t& kept_cnt) {
+                             unsigned long long s_all, float x_lo, bool record, uint64_t pol,
+                             AdjShared& A, uint32_t& key, unsigned long long& kept,
+                             uint32_t& kept_cnt, int& ncand) {
   const int tid = threadIdx.x;
   const uint32_t ktop = key16(M);
   for (int j = tid; j < kAdjBins1; j += NT) A.cnt1[j] = 0u;
+  if (tid == 0) A.ncand = 0;
   __syncthreads();
-  adj_visit_vec<__nv_bfloat16, NT>(row, V, vec, pol, [&](const float* x, int n) {
+  adj_visit_vec<__nv_bfloat16, NT>(row, V, vec, pol, [&](const float* x, int n, int v0) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       if (e < n && x[e] >= x_lo) {
         // x <= M, and x >= x_lo bounds the key from below: j < 2048 (guard only)
         const uint32_t j = ktop - key16(x[e]);
         atomicAdd(&A.cnt1[j < (uint32_t)kAdjBins1 ? j : kAdjBins1 - 1], 1u);
+        if (record) {
+          const int pos = atomicAdd(&A.ncand, 1);
+          if (pos < kAdjCand) A.cand[pos] = make_uint2((uint32_t)(v0 + e), __float_as_uint(x[e]));
+        }
       }
     }
   });
   __syncthreads();
+  ncand = (record && A.ncand <= kAdjCand) ? A.ncand : -1;
   for (int j = tid; j < kAdjBins1; j += NT) {
     const uint32_t n = A.cnt1[j];
     A.mass1[j] =
@@ -1412,12 +1451,13 @@ __device__ bool adj_estimate(const TT* row, int V, bool vec, float M, float c, f
 // Block-wide (every thread of the block calls it with the same arguments).
 // Returns false, leaving tau, S and kept_cnt alone, when no threshold exists
 // (NaN rows).
-// (mt, st + lt): this thread's sweep-1 max and compensated sum.
+// (mt, st + lt): this thread's sweep-1 max and compensated sum.  ncand: the
+// number of entries in A.cand when they include every kept entry, else -1.
 template <typename TT, int NT>
 __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M, float c, int top_k,
                            float top_p, bool use_k, bool use_p, float mt, float st, float lt,
                            uint64_t pol, AdjShared& A, float& tau, float& S, uint32_t& kept_cnt,
-                           unsigned long long* ctr) {
+                           int& ncand, unsigned long long* ctr) {
   // masses are pow2_neg(z) * 2^F with V * 2^F <= 2^62
   const int F = adj_mass_shift(V);
   const float fscale = adj_mass_scale(F);
@@ -1426,8 +1466,38 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
   unsigned long long kept = 0ull;
   AdjGrid g{64.0f, 0.0f, true}, gw{64.0f, 0.0f, true};
   bool ok = false;
+  ncand = -1;
   adj_count(ctr, kAdjRows);
-  if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g, gw)) {
+  if constexpr (sizeof(TT) == 2) {
+    if (use_k && top_k <= NT) {
+      // The threads' sweep-1 maxima are top_k or more distinct entries at or
+      // above the value where their count, from the top, reaches top_k: the
+      // top-k edge (and a top-p edge, which lies inside the top-k set) is at or
+      // above it.  The counting pass from there sees little more than the
+      // top-k set and lists it for sweep 2.
+      const uint32_t ktop = key16(M);
+      for (int j = threadIdx.x; j < kAdjBins1; j += NT) A.cnt1[j] = 0u;
+      __syncthreads();
+      if (mt > -INFINITY) {
+        const uint32_t j = ktop - key16(mt);  // mt <= M
+        atomicAdd(&A.cnt1[j < (uint32_t)kAdjBins1 ? j : kAdjBins1 - 1], 1u);
+      }
+      __syncthreads();
+      adj_select<NT>(A.cnt1, A.mass1, kAdjBins1, false, (uint32_t)top_k, 0.0, 0ull, A);
+      const int sel = A.sel;
+      __syncthreads();
+      if (sel < kAdjBins1 - 1) {
+        ok = adj_run_keys<NT>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
+                              top_k, top_p, use_k, use_p, 0ull, key16_value(ktop - sel), true,
+                              pol, A, key, kept, kc, ncand);
+        if (ok) adj_count(ctr, kAdjExact);
+        else ncand = -1;
+      }
+    }
+  }
+  if (ok) {
+    // resolved from the threads' maxima
+  } else if (adj_estimate<TT, NT>(row, V, vec, M, c, S, top_k, top_p, use_k, use_p, pol, A, g, gw)) {
     if constexpr (sizeof(TT) == 2) {
       // bins of one value each, down to the window's cut (or the cut grid's)
       const float x_lo = M - (gw.lo > 0.0f ? gw.cut : g.cut) / c;
@@ -1445,8 +1515,10 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
           s_all = adj_block_sum<NT>((unsigned long long)part, A);
         }
         if (fin) {
+          int nc;
           ok = adj_run_keys<NT>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
-                                top_k, top_p, use_k, use_p, s_all, x_lo, pol, A, key, kept, kc);
+                                top_k, top_p, use_k, use_p, s_all, x_lo, false, pol, A, key, kept,
+                                kc, nc);
           if (ok) adj_count(ctr, kAdjExact);
         }
       }
@@ -1583,13 +1655,15 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     for (int w = 0; w < NW; ++w) softmax_merge(M, S, red[par][w].x, red[par][w].y, P.c);
     float tau = -INFINITY;
     uint32_t kept_cnt = (uint32_t)V;
+    int ncand = -1;  // adjusted rows: kept entries all in the candidate list
     if constexpr (kAdj) {
       const int kk = P.topk ? __ldg(P.topk + b) : 0;
       const float pp = P.topp ? __ldg(P.topp + b) : 1.0f;
       const bool use_k = kk >= 1 && kk < V, use_p = !(pp >= 1.0f);
       if ((use_k || use_p) && M > -INFINITY && M < INFINITY)
         adjust_row<TT, NT>(row, V, vec, M, P.c, kk, pp, use_k, use_p, mt, st, l0, keep,
-                           *reinterpret_cast<AdjShared*>(adj_smem), tau, S, kept_cnt, P.adj_ctr);
+                           *reinterpret_cast<AdjShared*>(adj_smem), tau, S, kept_cnt, ncand,
+                           P.adj_ctr);
     }
     // few kept entries: at most 1/8 of the 16-byte vectors hold one, so sweep 2
     // skips the others (and their draft entries) instead of streaming them
@@ -1623,7 +1697,16 @@ __global__ void __launch_bounds__(NT, MINB) sweep_row_kernel(const Params P) {
     // row again, with x removed from a correction's residual)
     float beta = 0.0f;
     Race best = race_none();
-    if (has_q && !onehot && race)
+    if (kAdj && ncand >= 0) {
+      const uint2* cand = reinterpret_cast<const AdjShared*>(adj_smem)->cand;
+      if (has_q && !onehot && race)
+        sweep2_list<NT, true, true>(cand, ncand, qrow, M, P.c, invS, tau, resid, rkey, beta, best, -1);
+      else if (has_q && !onehot)
+        sweep2_list<NT, true, false>(cand, ncand, qrow, M, P.c, invS, tau, resid, rkey, beta, best, -1);
+      else if (race)
+        sweep2_list<NT, false, true>(cand, ncand, qrow, M, P.c, invS, tau, resid, rkey, beta, best,
+                                     resid ? s_x : -1);
+    } else if (has_q && !onehot && race)
       sweep2<TT, NT, true, true, kAdj>(row, qrow, 0, hi, vec, M, P.c, invS, tau, resid, rkey, drop,
                                        beta, best, -1, sparse);
     else if (has_q && !onehot)
