@@ -329,6 +329,52 @@ def adjust_settings(w, args, device, config=None):
     return make_top_k_top_p(w.B, w.V, seed=0, top_k=args.top_k, top_p=args.top_p, device=device)
 
 
+def adjusted_needed_bytes(w, tk, tp, chunk: int = 128) -> int:
+    """Bytes an adjusted step must read at the least: every target row once,
+    and of each draft row only the 32-byte sectors holding an entry of its
+    adjusted target's kept set (p' = 0 elsewhere, so neither beta nor the
+    residual needs q there).  The kept sets follow the definitions (top-k keeps
+    the ties at the k-th largest logit; top-p keeps v when the mass strictly
+    above it is below P times the top-k set's mass, or is 0), computed in
+    float64 with torch on the workload's device, outside any timed region."""
+    import torch
+    esize = 2 if w.dtype == "bf16" else 4
+    need = w.n_target * w.V * esize
+    if w.draft_probs is None or w.n_draft == 0:
+        return need
+    dev = w.target_logits.device
+    V = w.V
+    gam = (w.cu[1:] - w.cu[:-1]).long().to(dev)
+    req = torch.repeat_interleave(torch.arange(w.B, device=dev), gam)
+    trow = torch.arange(w.n_draft, device=dev) + req
+    tk, tp = tk.to(dev), tp.to(dev)
+    sectors = 0
+    for d0 in range(0, w.n_draft, chunk):
+        d1 = min(w.n_draft, d0 + chunk)
+        x = w.target_logits[trow[d0:d1]].double() / w.T
+        k = tk[req[d0:d1]].long()
+        p = tp[req[d0:d1]].double()
+        vals, order = torch.sort(x, dim=1, descending=True)
+        e = torch.exp(vals - vals[:, :1])
+        use_k = (k >= 1) & (k < V)
+        thr = vals.gather(1, (k - 1).clamp(0, V - 1)[:, None])[:, 0]
+        thr = torch.where(use_k, thr, torch.full_like(thr, -float("inf")))
+        keep = vals >= thr[:, None]
+        ek = e * keep
+        s_k = ek.sum(1)
+        neg = (-vals).contiguous()
+        first = torch.searchsorted(neg, neg)          # first index of each value's group
+        above = (torch.cumsum(ek, 1) - ek).gather(1, first)
+        use_p = ~(p >= 1.0)
+        in_p = (above < (p.clamp(min=0.0) * s_k)[:, None]) | (above == 0)
+        keep &= in_p | ~use_p[:, None]
+        sec = torch.zeros(d1 - d0, (V + 7) // 8, dtype=torch.int32, device=dev)
+        sec.scatter_add_(1, order // 8, keep.int())
+        sectors += int((sec > 0).sum())
+        del x, vals, order, e, keep, ek, neg, first, above, sec
+    return need + 32 * sectors
+
+
 def adjust_desc(args):
     if args.adjust_mix:
         return "seeded per-request mix"
@@ -470,6 +516,7 @@ def measure(args, dist, dev, sd, config: int, steps: int, warmup: int) -> Measur
     peak, peak_kind = measured_peak_gbs()
     achieved = alg_bytes_rows / (row_avg_ms / 1e3) / 1e9
     traffic = recorded_traffic(workload_key, kernel_name, alg_bytes_rows)
+    needed = adjusted_needed_bytes(w, tk, tp) if tk is not None else None
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
@@ -494,6 +541,13 @@ def measure(args, dist, dev, sd, config: int, steps: int, warmup: int) -> Measur
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
+    if needed is not None:
+        # adjusted rows need q only where p' > 0: rows that keep few entries
+        # (top-k) read far less than a whole draft row, so the row kernel can
+        # exceed the roofline of the every-row figure above; this is its rate
+        # against the bytes such a step must read at the least
+        result["roofline"]["needed_bytes_per_launch"] = needed
+        result["roofline"]["frac_of_needed"] = needed / (row_avg_ms / 1e3) / 1e9 / peak
     return Measured(result=result, v=v, w=w, out=out, stream=stream, offset=offset, tk=tk, tp=tp,
                     step=step)
 

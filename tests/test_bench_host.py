@@ -153,3 +153,34 @@ def test_gpu_local_cpus_from_topology_table():
     assert bench.gpu_local_cpus(2, topo) == (None, None)
     assert bench.gpu_local_cpus(0, "garbage") == (None, None)
     assert bench.parse_cpu_list("0-3,8,10-11") == {0, 1, 2, 3, 8, 10, 11}
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_adjusted_needed_bytes_by_brute_force(seed):
+    # every target row, plus 32 bytes per draft-row sector holding a kept entry;
+    # kept sets written out from the definitions, one entry at a time
+    import numpy as np
+    from speculative_decoding_rejection_decode_gb300.inputs import make_top_k_top_p, make_workload
+    w = make_workload(name="t", B=7, gamma=(0, 4), V=40, dtype="bf16", T=0.7, seed=seed,
+                      target_std=1.0)
+    tk, tp = make_top_k_top_p(w.B, w.V, seed=5 + seed)
+    got = bench.adjusted_needed_bytes(w, tk, tp, chunk=3)
+    cu, V, sectors = w.cu.tolist(), w.V, 0
+    for b in range(w.B):
+        for i in range(cu[b + 1] - cu[b]):
+            x = w.target_logits[cu[b] + b + i].double().numpy() / w.T
+            k, p = int(tk[b]), float(tp[b])
+            e = np.exp(x - x.max())
+            keep = np.ones(V, bool)
+            if 1 <= k < V:
+                keep = x >= np.sort(x)[::-1][k - 1]
+            s_k = e[keep].sum()
+            if not p >= 1.0:
+                above = np.array([e[keep & (x > x[v])].sum() for v in range(V)])
+                keep &= (above < max(p, 0.0) * s_k) | (above == 0)
+            sectors += len(set((np.nonzero(keep)[0] // 8).tolist()))
+    assert got == w.n_target * V * 2 + 32 * sectors
+    # without settings every kept set is the whole row: every sector of every draft row
+    none_k, none_p = make_top_k_top_p(w.B, w.V, 0, top_k=0, top_p=1.0)
+    assert bench.adjusted_needed_bytes(w, none_k, none_p) == w.n_target * V * 2 + \
+        w.n_draft * 32 * ((V + 7) // 8)

@@ -140,6 +140,23 @@ def test_ties_signed_zero_and_masked_entries(V, dtype):
         _check(V, w, tk, tp)
 
 
+@pytest.mark.parametrize("spread", [2, 40])
+def test_top_k_with_large_tie_groups(V, spread):
+    # bf16 integer logits in [-spread, spread]: with spread 2 the top value alone
+    # holds ~13000 entries of each row, more than the candidate list of a top-k
+    # row takes (the row falls back to sweeping the whole row); with spread 40
+    # the list holds the top groups; both must keep every entry of the edge group
+    g0 = torch.Generator().manual_seed(spread)
+    B, gam, Vs = 8, 3, 65536
+    tgt = torch.randint(-spread, spread + 1, (B * (gam + 1), Vs), generator=g0).float().bfloat16()
+    q = torch.softmax(torch.randn(B * gam, Vs, generator=g0), -1)
+    ids = torch.multinomial(q, 1, generator=g0).view(-1).int()
+    w = from_rows(tgt, q, ids, [gam] * B, T=1.0, seed=21).to("cuda")
+    for k in (1, 20, 500):
+        _check(V, w, *make_top_k_top_p(B, Vs, 0, top_k=k))
+    _check(V, w, *make_top_k_top_p(B, Vs, 0, top_k=20, top_p=0.5))
+
+
 def test_onehot_drafts_with_settings(V):
     w = make_workload(name="adj onehot", B=48, gamma=(0, 7), V=50000, dtype="bf16", T=1.0,
                       seed=77, ids="argmax0.75", device="cuda")
