@@ -1975,9 +1975,10 @@ struct alignas(16) PairShared {
   int gmax, bad, flag;
 };
 
-template <typename TT>
-__global__ void __launch_bounds__(512, 2) pair_row_kernel(const Params P) {
-  constexpr int NT = 512, NW = 16;
+template <typename TT, int NT = 512>
+__global__ void __launch_bounds__(NT, 1024 / NT) pair_row_kernel(const Params P) {
+  constexpr int NW = NT / 32;
+  static_assert(NW <= 16, "PairShared::red holds 16 warps");
   constexpr int kEl = 16 / sizeof(TT);
   __shared__ PairShared S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -60,11 +60,13 @@ struct specdec_ctx {
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
   int stream_smem[4] = {0, 0, 0, 0};  // dynamic shared memory set on stream_row_kernel<dtype, ctas>
   int smem_per_sm = 0;
-  int sweep_threads = 512;      // block size of the sweep kernel (1024 x 1, 512 x 2, 256 x 4 per SM)
+  int sweep_threads = 0;        // block size of the sweep kernel (1024 x 1 .. 64 x 16 per SM; 0: by call)
   int stream_ctas = 1;          // stream kernel CTAs per SM (1 or 2)
-  int pair_clusters[2] = {0, 0};  // co-resident 2-CTA clusters of pair_row_kernel<f32 / bf16>
+  int pair_clusters[2][2] = {{0, 0}, {0, 0}};  // co-resident 2-CTA clusters of pair_row_kernel<f32 / bf16, 512 / 256>
+  int pair_threads = 512;           // pair kernel block size (512: 2 CTAs per SM, or 256: 4)
   int occ_cache[2][5][2] = {};  // [dtype][cluster index] -> {smem, clusters}
-  int adj_smem_set[2] = {0, 0};  // dynamic shared memory set on the adjusted sweep kernel
+  int adj_smem_set[2][2] = {{0, 0}, {0, 0}};  // dynamic shared memory set on the adjusted sweep kernel
+  int adj_threads = 512;            // adjusted sweep kernel block size (512: 2 CTAs per SM, or 1024: 1)
   unsigned long long* adj_ctr = nullptr;  // caller's selection counters (profiling), or null
   int fault_mode = 0;           // specdec_set_fault_injection
   uint64_t fault_wait_ns = 0;
@@ -243,7 +245,9 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
   const int B = P.B;
   if (h->ev_before) cudaEventRecord(h->ev_before, st);
   if (path == SPECDEC_PATH_PAIR) {
-    int& nclus = h->pair_clusters[sizeof(TT) == 2];
+    const bool small = h->pair_threads == 256;
+    auto kern = small ? pair_row_kernel<TT, 256> : pair_row_kernel<TT, 512>;
+    int& nclus = h->pair_clusters[sizeof(TT) == 2][small];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -252,19 +256,19 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(512);
+    cfg.blockDim = dim3(h->pair_threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     if (nclus == 0) {
       cfg.gridDim = dim3(2 * h->num_sms);
-      if (cudaOccupancyMaxActiveClusters(&nclus, pair_row_kernel<TT>, &cfg) != cudaSuccess || nclus <= 0) {
+      if (cudaOccupancyMaxActiveClusters(&nclus, kern, &cfg) != cudaSuccess || nclus <= 0) {
         cudaGetLastError();
         nclus = 0;
         return SPECDEC_ERR_CUDA;
       }
     }
     cfg.gridDim = dim3(2 * nclus);
-    if (cudaLaunchKernelEx(&cfg, pair_row_kernel<TT>, P) != cudaSuccess) return SPECDEC_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) return SPECDEC_ERR_CUDA;
   } else if (path == SPECDEC_PATH_STREAM) {
     const int ctas = h->stream_ctas;
     const int fixed = (int)((sizeof(StreamShared) + 127) / 128 * 128);
@@ -284,22 +288,33 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
     dual_row_kernel<TT><<<h->num_sms * 2, 512, 0, st>>>(P);
   } else if (path == SPECDEC_PATH_SWEEP) {
     if (P.topk || P.topp) {
-      auto kern = sweep_row_kernel<TT, 512, 2, true>;
-      int& set = h->adj_smem_set[sizeof(TT) == 2];
+      const bool one = h->adj_threads == 1024;
+      auto kern = one ? sweep_row_kernel<TT, 1024, 1, true> : sweep_row_kernel<TT, 512, 2, true>;
+      int& set = h->adj_smem_set[sizeof(TT) == 2][one];
       if (!set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(AdjShared)) != cudaSuccess)
           return SPECDEC_ERR_CUDA;
         set = 1;
       }
-      kern<<<h->num_sms * 2, 512, sizeof(AdjShared), st>>>(P);
+      kern<<<h->num_sms * (one ? 1 : 2), one ? 1024 : 512, sizeof(AdjShared), st>>>(P);
     }
-    else if (h->sweep_threads == 512)
-      sweep_row_kernel<TT, 512, 2><<<h->num_sms * 2, 512, 0, st>>>(P);
-    else if (h->sweep_threads == 256)
-      sweep_row_kernel<TT, 256, 4><<<h->num_sms * 4, 256, 0, st>>>(P);
-    else
-      sweep_row_kernel<TT, 1024, 1><<<h->num_sms, 1024, 0, st>>>(P);
+    else {
+      // Draft rows given: two 512-thread CTAs per SM.  One-hot drafts: eight
+      // 128-thread CTAs, so that while some CTAs draw a race (ALU work on a
+      // row in L2) the others keep streaming rows from HBM.
+      const int th = h->sweep_threads ? h->sweep_threads : (P.q ? 512 : 128);
+      if (th == 512)
+        sweep_row_kernel<TT, 512, 2><<<h->num_sms * 2, 512, 0, st>>>(P);
+      else if (th == 256)
+        sweep_row_kernel<TT, 256, 4><<<h->num_sms * 4, 256, 0, st>>>(P);
+      else if (th == 128)
+        sweep_row_kernel<TT, 128, 8><<<h->num_sms * 8, 128, 0, st>>>(P);
+      else if (th == 64)
+        sweep_row_kernel<TT, 64, 16><<<h->num_sms * 16, 64, 0, st>>>(P);
+      else
+        sweep_row_kernel<TT, 1024, 1><<<h->num_sms, 1024, 0, st>>>(P);
+    }
   } else if (path == SPECDEC_PATH_FUSED) {
     P.slice_len = f.slice_len;
     P.tbuf_bytes = f.tbuf_bytes;
@@ -360,10 +375,19 @@ int specdec_create(specdec_handle_t* out, int device) {
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   cudaDeviceGetAttribute(&h->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
-  // tuning knobs for measurements: sweep block size (1024, 512, 256) and stream CTAs per SM
+  // tuning knobs for measurements: sweep block size (1024 .. 64), adjusted sweep block
+  // size (512, 1024), pair block size (512, 256) and stream CTAs per SM
   if (const char* e = std::getenv("SPECDEC_SWEEP_THREADS")) {
     const int v = std::atoi(e);
-    if (v == 256 || v == 512 || v == 1024) h->sweep_threads = v;
+    if (v == 64 || v == 128 || v == 256 || v == 512 || v == 1024) h->sweep_threads = v;
+  }
+  if (const char* e = std::getenv("SPECDEC_ADJ_THREADS")) {
+    const int v = std::atoi(e);
+    if (v == 512 || v == 1024) h->adj_threads = v;
+  }
+  if (const char* e = std::getenv("SPECDEC_PAIR_THREADS")) {
+    const int v = std::atoi(e);
+    if (v == 256 || v == 512) h->pair_threads = v;
   }
   if (const char* e = std::getenv("SPECDEC_STREAM_CTAS")) {
     const int v = std::atoi(e);
