@@ -25,7 +25,9 @@
  * `seed` (SplitMix64 of Steele, Lea and Flood, OOPSLA 2014):
  *     sm(z)  = SplitMix64 finaliser applied to z + 0x9E3779B97F4A7C15
  *     key    = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream))
- *     U      = ((sm(key ^ v) >> 41) + 0.5) * 2^-23          (exact in float32)
+ *     h      = sm(key ^ (v >> 1))      (one hash for the pair of entries 2j, 2j + 1)
+ *     U      = ((h >> 41) + 0.5) * 2^-23                 for even v
+ *     U      = (((h >> 18) & (2^23 - 1)) + 0.5) * 2^-23  for odd v   (exact in float32)
  * r_i = U(seed, b, i, stream 0, v 0); the extra token is the exponential race
  * t = argmax_v w(v) / E_v with E_v = -ln U(seed, b, n_b, stream 1, v), an exact
  * sampler of norm(w) that needs no normaliser and no prefix scan.

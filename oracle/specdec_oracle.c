@@ -70,8 +70,11 @@
  * Counter-based generator (the pages only say "uniform random"): SplitMix64
  * (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
  * OOPSLA 2014; the finaliser as published by Vigna) keyed by
- *     k = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream)),  h = sm(k ^ v),
- *     U = ((h >> 41) + 0.5) * 2^-23    (23 bits, strictly inside (0, 1)).
+ *     k = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream)),  h = sm(k ^ (v >> 1)),
+ *     U = ((h >> 41) + 0.5) * 2^-23               for even v,
+ *     U = (((h >> 18) mod 2^23) + 0.5) * 2^-23     for odd v
+ * (23 bits, strictly inside (0, 1); one 64-bit output serves the two entries
+ * 2j and 2j + 1 with disjoint bit fields).
  * stream 0 / v 0 is the accept uniform r_i of draft position pos; stream 1 / v
  * is the race uniform of vocabulary entry v at output position pos.  U equals
  * (2k+1) 2^-24 with 2k+1 < 2^24, an exact float and an exact double, so both
@@ -124,8 +127,9 @@ uint64_t oracle_stream_key(uint64_t seed, uint64_t b, uint64_t pos, uint64_t str
 }
 
 double oracle_uniform(uint64_t seed, uint64_t b, uint64_t pos, uint64_t stream, uint64_t v) {
-  uint64_t h = oracle_splitmix64(oracle_stream_key(seed, b, pos, stream) ^ v);
-  return ((double)(h >> 41) + 0.5) * (1.0 / 8388608.0);
+  const uint64_t h = oracle_splitmix64(oracle_stream_key(seed, b, pos, stream) ^ (v >> 1));
+  const uint64_t bits = (v & 1) ? ((h >> 18) & 0x7FFFFFULL) : (h >> 41);
+  return ((double)bits + 0.5) * (1.0 / 8388608.0);
 }
 
 /* Fills out[j] = U(seed, b, pos, stream, v0 + j) for j < n (used by tests). */

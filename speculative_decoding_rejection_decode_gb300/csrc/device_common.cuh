@@ -32,9 +32,18 @@ __host__ __device__ __forceinline__ uint64_t stream_key(uint64_t seed, uint64_t 
   return splitmix64(splitmix64(splitmix64(seed) ^ b) ^ ((pos << 8) | stream));
 }
 
-// Top 23 bits of the hash of (key ^ v): U = (k + 1/2) 2^-23, k in [0, 2^23).
+// 23 bits for entry v: one hash of (key ^ (v >> 1)) serves the pair (2j, 2j+1),
+// bits [41, 64) for even v and bits [18, 41) for odd v; U = (k + 1/2) 2^-23,
+// k in [0, 2^23).
 __device__ __forceinline__ uint32_t uniform_bits(uint64_t key, uint64_t v) {
-  return (uint32_t)(splitmix64(key ^ v) >> 41);
+  const uint64_t h = splitmix64(key ^ (v >> 1));
+  return (v & 1) ? (uint32_t)(h >> 18) & 0x7FFFFFu : (uint32_t)(h >> 41);
+}
+// Both uniforms of the pair (2j, 2j + 1) from their one hash.
+__device__ __forceinline__ void uniform_bits2(uint64_t key, uint64_t j, uint32_t& k0, uint32_t& k1) {
+  const uint64_t h = splitmix64(key ^ j);
+  k0 = (uint32_t)(h >> 41);
+  k1 = (uint32_t)(h >> 18) & 0x7FFFFFu;
 }
 
 __device__ __forceinline__ float uniform_from_bits(uint32_t k) {
@@ -110,14 +119,19 @@ __device__ __forceinline__ float one_minus_uniform(uint32_t k) {
   return (float)((1u << 24) - 2u * k - 1u) * (1.0f / 16777216.0f);  // exact
 }
 
-// Offers entries v .. v+3 with weights w[0..3]: the four hashes are independent
+// Offers entries v .. v+3 with weights w[0..3]: the hashes are independent
 // (no branch between them); only entries that pass the bound take the log and
 // the comparison.  Checking all four against the best from before the group is
 // conservative, so the result is the one race_offer gives one by one.
 __device__ __forceinline__ void race_offer4(Race& a, const float* w, uint64_t key, uint32_t v) {
   uint32_t k[4];
+  if ((v & 1u) == 0u) {  // two pairs: two hashes (every caller's v is a multiple of 4)
+    uniform_bits2(key, v >> 1, k[0], k[1]);
+    uniform_bits2(key, (v >> 1) + 1, k[2], k[3]);
+  } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) k[i] = uniform_bits(key, v + i);
+    for (int i = 0; i < 4; ++i) k[i] = uniform_bits(key, v + i);
+  }
   bool c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) c[i] = w[i] > 0.0f && !race_hopeless(a, w[i], one_minus_uniform(k[i]));

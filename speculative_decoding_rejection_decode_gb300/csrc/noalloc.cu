@@ -163,12 +163,21 @@ extern "C" int specdec_rejection_sample_noalloc(
                reinterpret_cast<uintptr_t>(draft_probs) % 16 == 0;
     const int race_grid = sms * 8;
     cudaError_t e;
+    // one-hot drafts: eight 128-thread CTAs per SM (racing CTAs and streaming
+    // ones share each SM), as on the handle path
+    const bool onehot = draft_probs == nullptr;
     if (dtype == SPECDEC_BF16) {
-      sweep_row_kernel<__nv_bfloat16, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
+      if (onehot)
+        sweep_row_kernel<__nv_bfloat16, 128, 8><<<sms * 8, 128, 0, st>>>(P);
+      else
+        sweep_row_kernel<__nv_bfloat16, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
       e = launch_dependent(finalize_kernel, (B + 255) / 256, 256, st, P);
       if (e == cudaSuccess) e = launch_dependent(race_kernel<__nv_bfloat16>, race_grid, kRowThreads, st, P);
     } else {
-      sweep_row_kernel<float, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
+      if (onehot)
+        sweep_row_kernel<float, 128, 8><<<sms * 8, 128, 0, st>>>(P);
+      else
+        sweep_row_kernel<float, kThreads, 2><<<sms * 2, kThreads, 0, st>>>(P);
       e = launch_dependent(finalize_kernel, (B + 255) / 256, 256, st, P);
       if (e == cudaSuccess) e = launch_dependent(race_kernel<float>, race_grid, kRowThreads, st, P);
     }

@@ -44,13 +44,35 @@ def test_uniform_chi_square_2_pow_20():
 
 
 def test_key_composition():
-    # k = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream)); h = sm(k ^ v).
+    # k = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream)); h = sm(k ^ (v >> 1)) serves
+    # entries 2j and 2j + 1: bits 41..63 for the even one, bits 18..40 for the odd.
     sm = oracle.splitmix64
     seed, b, pos, stream, v = 0xDEADBEEF, 17, 5, 1, 123456
     k = sm(sm(sm(seed) ^ b) ^ ((pos << 8) | stream))
     assert oracle.stream_key(seed, b, pos, stream) == k
-    h = sm(k ^ v)
+    h = sm(k ^ (v >> 1))
     assert oracle.uniform(seed, b, pos, stream, v, 1)[0] == ((h >> 41) + 0.5) / 2**23
+    assert oracle.uniform(seed, b, pos, stream, v + 1, 1)[0] == \
+        (((h >> 18) & (2**23 - 1)) + 0.5) / 2**23
+    # the accept uniform (stream 0, v = 0) is the top of sm(k ^ 0)
+    k0 = oracle.stream_key(seed, b, pos, 0)
+    assert oracle.uniform(seed, b, pos, 0, 0, 1)[0] == ((sm(k0) >> 41) + 0.5) / 2**23
+
+
+def test_pair_halves_are_independent_uniforms():
+    # The two entries of a pair come from disjoint bit fields of one output:
+    # each field is uniform on its own and the pair is uniform on the unit
+    # square (a field that overlapped the other, or a wrong shift, fails here).
+    u = oracle.uniform(2024, 3, 1, 1, 0, 1 << 19)
+    even, odd = u[0::2], u[1::2]
+    for x in (even, odd):
+        hist, _ = np.histogram(x, bins=128, range=(0.0, 1.0))
+        assert stats.chisquare(hist).pvalue > 1e-3
+    h2, _, _ = np.histogram2d(even, odd, bins=16, range=[[0, 1], [0, 1]])
+    assert stats.chisquare(h2.ravel()).pvalue > 1e-3
+    assert abs(np.corrcoef(even, odd)[0, 1]) < 0.01
+    # neighbouring pairs are unrelated too
+    assert abs(np.corrcoef(odd[:-1], even[1:])[0, 1]) < 0.01
 
 
 def test_stored_vectors_match():
@@ -62,4 +84,5 @@ def test_stored_vectors_match():
         seed, b, pos, stream, v, h_hex, u = line.split()
         seed, b, pos, stream, v = (int(x, 0) for x in (seed, b, pos, stream, v))
         assert oracle.uniform(seed, b, pos, stream, v, 1)[0] == float.fromhex(u)
-        assert oracle.splitmix64(oracle.stream_key(seed, b, pos, stream) ^ v) == int(h_hex, 16)
+        assert oracle.splitmix64(oracle.stream_key(seed, b, pos, stream) ^ (v >> 1)) == \
+            int(h_hex, 16)
