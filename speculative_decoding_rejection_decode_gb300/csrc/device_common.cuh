@@ -229,16 +229,25 @@ constexpr int kPrefixUnknown = 0;
 constexpr int kPrefixAllAccepted = 1;
 constexpr int kPrefixRejected = 2;
 
+// The status words are read eight at a time, all loads issued before any is
+// looked at, so a prefix of i positions costs about ceil(i / 8) load latencies
+// (the thread that takes a work slot waits on this while its CTA idles).
 __device__ __forceinline__ int read_prefix(const uint64_t* status, int64_t t_first, int i,
                                            uint64_t epoch) {
   int state = kPrefixAllAccepted;
-  for (int j = 0; j < i; ++j) {
-    uint64_t s = ld_relaxed_u64(status + t_first + j);
-    if ((s >> 8) != epoch || !(s & kStDone)) {
-      state = kPrefixUnknown;
-      continue;
+  for (int j0 = 0; j0 < i; j0 += 8) {
+    uint64_t s[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = j0 + j < i ? ld_relaxed_u64(status + t_first + j0 + j) : 0ull;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j0 + j >= i) break;
+      if ((s[j] >> 8) != epoch || !(s[j] & kStDone)) {
+        state = kPrefixUnknown;
+        continue;
+      }
+      if (!(s[j] & kStAccepted)) return kPrefixRejected;
     }
-    if (!(s & kStAccepted)) return kPrefixRejected;
   }
   return state;
 }

@@ -61,6 +61,7 @@ struct specdec_ctx {
   int stream_smem[4] = {0, 0, 0, 0};  // dynamic shared memory set on stream_row_kernel<dtype, ctas>
   int smem_per_sm = 0;
   int sweep_threads = 0;        // block size of the sweep kernel (1024 x 1 .. 64 x 16 per SM; 0: by call)
+  int sweep_ctas = 0;           // grid of the 512-thread sweep kernel (0: two per SM)
   int stream_ctas = 1;          // stream kernel CTAs per SM (1 or 2)
   int pair_clusters[2][2] = {{0, 0}, {0, 0}};  // co-resident 2-CTA clusters of pair_row_kernel<f32 / bf16, 512 / 256>
   int pair_threads = 512;           // pair kernel block size (512: 2 CTAs per SM, or 256: 4)
@@ -305,7 +306,7 @@ int launch_sampling(specdec_ctx* h, Params& P, const FusedConfig& f, int path, c
       // row in L2) the others keep streaming rows from HBM.
       const int th = h->sweep_threads ? h->sweep_threads : (P.q ? 512 : 128);
       if (th == 512)
-        sweep_row_kernel<TT, 512, 2><<<h->num_sms * 2, 512, 0, st>>>(P);
+        sweep_row_kernel<TT, 512, 2><<<h->sweep_ctas ? h->sweep_ctas : h->num_sms * 2, 512, 0, st>>>(P);
       else if (th == 256)
         sweep_row_kernel<TT, 256, 4><<<h->num_sms * 4, 256, 0, st>>>(P);
       else if (th == 128)
@@ -375,11 +376,15 @@ int specdec_create(specdec_handle_t* out, int device) {
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   cudaDeviceGetAttribute(&h->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
-  // tuning knobs for measurements: sweep block size (1024 .. 64), adjusted sweep block
+  // tuning knobs for measurements: sweep block size (1024 .. 64) and grid, adjusted sweep block
   // size (512, 1024), pair block size (512, 256) and stream CTAs per SM
   if (const char* e = std::getenv("SPECDEC_SWEEP_THREADS")) {
     const int v = std::atoi(e);
     if (v == 64 || v == 128 || v == 256 || v == 512 || v == 1024) h->sweep_threads = v;
+  }
+  if (const char* e = std::getenv("SPECDEC_SWEEP_CTAS")) {
+    const int v = std::atoi(e);
+    if (v >= 1 && v <= 2 * h->num_sms) h->sweep_ctas = v;
   }
   if (const char* e = std::getenv("SPECDEC_ADJ_THREADS")) {
     const int v = std::atoi(e);
