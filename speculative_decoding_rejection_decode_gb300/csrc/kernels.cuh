@@ -2022,39 +2022,44 @@ __global__ void __launch_bounds__(NT, 1024 / NT) pair_row_kernel(const Params P)
   const uint64_t limit = P.wait_ns ? P.wait_ns : kWaitLimitNs;
   bool ok = true;
 
+  // ---- rank 0 takes a slot and sends it to both CTAs' desc[p] -------------
+  // Row k + 1's slot is taken by thread 32 of rank 0 right after row k's final
+  // block barrier, while thread 0 still combines the halves and writes row k's
+  // outputs, so the two latencies overlap.
+  auto grab = [&](int p, bool first) {
+    long long u;
+    int prefix = kPrefixAllAccepted;
+    while (true) {
+      u = (long long)atomicAdd(P.sched, 1ull);
+      if (u >= total) {
+        u = -1;
+        break;
+      }
+      const int i = (int)(u / B), b = (int)(u % B);
+      const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
+      if (i > g) continue;
+      const int64_t t = (int64_t)c0 + b + i;
+      if (t >= P.cap_rows) {
+        set_err(P.err, SPECDEC_DEVERR_CAPACITY);
+        continue;
+      }
+      prefix = i > 0 ? read_prefix(P.status, t - i, i, P.epoch) : kPrefixAllAccepted;
+      if (i == g && prefix == kPrefixRejected) continue;  // bonus row nobody needs
+      break;
+    }
+    const uint32_t slot = smem_addr(&S.desc[p]);
+    for (uint32_t r = 0; r < 2; ++r) {
+      if (P.stall_peer && r == 1 && first) continue;  // test hook: rank 1 is left waiting
+      st_cluster_v4(mapa(slot, r), __int_as_float((int)(u & 0xFFFFFFFF)),
+                    __int_as_float((int)(u >> 32)), __int_as_float(prefix), 0.f);
+      mbar_arrive_cluster(mapa(smem_addr(&S.bdesc[p]), r));
+    }
+  };
+  if (rank == 0 && tid == 0) grab(0, true);
+
   for (uint32_t k = 0;; ++k) {
     const int par = k & 1;
     const uint32_t ph = (k >> 1) & 1;
-    // ---- rank 0 takes the next slot and sends it to both CTAs ---------------
-    if (rank == 0 && tid == 0) {
-      long long u;
-      int prefix = kPrefixAllAccepted;
-      while (true) {
-        u = (long long)atomicAdd(P.sched, 1ull);
-        if (u >= total) {
-          u = -1;
-          break;
-        }
-        const int i = (int)(u / B), b = (int)(u % B);
-        const int c0 = __ldg(P.cu + b), g = __ldg(P.cu + b + 1) - c0;
-        if (i > g) continue;
-        const int64_t t = (int64_t)c0 + b + i;
-        if (t >= P.cap_rows) {
-          set_err(P.err, SPECDEC_DEVERR_CAPACITY);
-          continue;
-        }
-        prefix = i > 0 ? read_prefix(P.status, t - i, i, P.epoch) : kPrefixAllAccepted;
-        if (i == g && prefix == kPrefixRejected) continue;  // bonus row nobody needs
-        break;
-      }
-      const uint32_t slot = smem_addr(&S.desc[par]);
-      for (uint32_t r = 0; r < 2; ++r) {
-        if (P.stall_peer && r == 1 && k == 0) continue;  // test hook: rank 1 is left waiting
-        st_cluster_v4(mapa(slot, r), __int_as_float((int)(u & 0xFFFFFFFF)),
-                      __int_as_float((int)(u >> 32)), __int_as_float(prefix), 0.f);
-        mbar_arrive_cluster(mapa(smem_addr(&S.bdesc[par]), r));
-      }
-    }
     if (tid == 0) S.flag = (ok && mbar_wait_cluster(smem_addr(&S.bdesc[par]), ph, limit)) ? 0 : 1;
     __syncthreads();
     if (S.flag) {
@@ -2149,6 +2154,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) pair_row_kernel(const Params P)
     warp_race(best);
     if (lane == 0) S.red[1][warp] = make_float4(beta, best.w, best.e, __int_as_float(best.idx));
     __syncthreads();
+    // both CTAs have read desc[par ^ 1] (row k - 1) before this row's first barrier
+    if (rank == 0 && tid == 32) grab(par ^ 1, false);
     if (tid == 0) {
       float bh = 0.0f;
       Race rh = race_none();
