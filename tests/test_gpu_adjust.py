@@ -157,6 +157,18 @@ def test_top_k_with_large_tie_groups(V, spread):
     _check(V, w, *make_top_k_top_p(B, Vs, 0, top_k=20, top_p=0.5))
 
 
+@pytest.mark.parametrize("frac_k,top_p", [(0.999, 1.0), (0.75, 1.0), (0.6, 0.9), (1.0, 0.95)])
+def test_top_k_keeping_most_of_the_row(V, frac_k, top_p):
+    # 2k > V: the edge lies near the bottom of the row (k = V - 1 drops the
+    # smallest value's group only when it holds one entry); with top-p the edge
+    # is chosen inside the top-k set
+    w = make_workload(name="adj large k", B=16, gamma=3, V=30000, dtype="bf16", T=1.0, seed=23,
+                      target_std=3.0, noise_std=0.8, device="cuda")
+    k = w.V - 1 if frac_k == 1.0 else int(frac_k * w.V)
+    tk, tp = make_top_k_top_p(w.B, w.V, 0, top_k=k, top_p=top_p)
+    _check(V, w, tk, tp)
+
+
 def test_onehot_drafts_with_settings(V):
     w = make_workload(name="adj onehot", B=48, gamma=(0, 7), V=50000, dtype="bf16", T=1.0,
                       seed=77, ids="argmax0.75", device="cuda")
@@ -274,6 +286,28 @@ def test_selection_counters(V):
     # every row that was verified was adjusted; none lacked a threshold
     assert c[0] >= w.B and c[0] <= w.n_target
     assert c[4] == 0
+    assert c[5] == 0                   # f32 rows: the general selection
     before = list(c)
     run_gpu_adj(V, w, tk, tp)          # counters off: unchanged
     assert ctr.cpu().tolist() == before
+
+
+@pytest.mark.parametrize("std,top_k,top_p,value_bins", [
+    (3.0, 50, 1.0, "all"),     # bf16, edge a few octaves below the max: one bin per value
+    (3.0, 0, 0.9, "all"),      # top-p alone: the bound from the compensated sweep-1 mass
+    (0.02, 0, 0.9, "none"),    # logits around 0: the values above the cut span > 2048 keys
+])
+def test_value_bins_and_general_selection_agree_with_oracle(V, std, top_k, top_p, value_bins):
+    w = make_workload(name="adj paths", B=16, gamma=3, V=40000, dtype="bf16", T=1.0, seed=19,
+                      target_std=std, noise_std=0.5, device="cuda")
+    tk, tp = make_top_k_top_p(w.B, w.V, 0, top_k=top_k, top_p=top_p)
+    ctr = torch.zeros(8, dtype=torch.int64, device="cuda")
+    V.set_adjust_counters(ctr)
+    _check(V, w, tk, tp)
+    V.set_adjust_counters(None)
+    c = ctr.cpu().tolist()
+    assert c[0] > 0 and c[4] == 0
+    if value_bins == "all":
+        assert c[5] == c[0]
+    else:
+        assert c[5] == 0
