@@ -64,7 +64,33 @@ __device__ __forceinline__ void tree_pass(const TT* row, const float* qrow, int 
     const uint4* rv = reinterpret_cast<const uint4*>(row);
     const uint4* qv = reinterpret_cast<const uint4*>(qrow);
     const int nv = V / kEl;
-    for (int j = tid; j < nv; j += NT) {
+    // U vectors (and their draft entries) in flight per thread, then the tail
+    constexpr int U = kRace ? 2 : 3;
+    int j = tid;
+    for (; j + (U - 1) * NT < nv; j += U * NT) {
+      uint4 a[U];
+      uint4 b[U][kEl / 4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        a[u] = ldg_hint(rv + j + u * NT, pol);
+        if constexpr (kHasQ) {
+#pragma unroll
+          for (int h = 0; h < kEl / 4; ++h) b[u][h] = ldg_hint(qv + (j + u * NT) * (kEl / 4) + h, pol);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float x[kEl];
+        unpack16<TT>(a[u], x);
+#pragma unroll
+        for (int h = 0; h < kEl / 4; ++h) {
+          float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (kHasQ) q4 = *reinterpret_cast<const float4*>(&b[u][h]);
+          four(x + 4 * h, q4, (uint32_t)((j + u * NT) * kEl + 4 * h));
+        }
+      }
+    }
+    for (; j < nv; j += NT) {
       float x[kEl];
       unpack16<TT>(ldg_hint(rv + j, pol), x);
 #pragma unroll
