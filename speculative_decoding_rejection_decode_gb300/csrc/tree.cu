@@ -65,7 +65,7 @@ __device__ __forceinline__ void tree_pass(const TT* row, const float* qrow, int 
     const uint4* qv = reinterpret_cast<const uint4*>(qrow);
     const int nv = V / kEl;
     // U vectors (and their draft entries) in flight per thread, then the tail
-    constexpr int U = kRace ? 2 : 3;
+    constexpr int U = kRace ? 2 : 4;
     int j = tid;
     for (; j + (U - 1) * NT < nv; j += U * NT) {
       uint4 a[U];
