@@ -1064,6 +1064,42 @@ __device__ __forceinline__ void adj_visit_vec(const TT* row, int V, bool vec, ui
   }
 }
 
+// As adj_visit_vec, with four vectors loaded before any is processed (the
+// counting pass of adj_run_keys reads rows that L2 has mostly let go, so it
+// needs more loads in flight than the passes served from L2).
+template <typename TT, int NT, typename Fn>
+__device__ __forceinline__ void adj_visit_vec4(const TT* row, int V, bool vec, uint64_t pol, Fn&& f) {
+  constexpr int kEl = 16 / sizeof(TT);
+  const int tid = threadIdx.x;
+  if (vec) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    const int nv = V / kEl;
+    int j = tid;
+    for (; j + 3 * NT < nv; j += 4 * NT) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = ldg_hint(rv + j + u * NT, pol);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float x[kEl];
+        unpack16<TT>(a[u], x);
+        f(x, kEl, (j + u * NT) * kEl);
+      }
+    }
+    for (; j < nv; j += NT) {
+      float x[kEl];
+      unpack16<TT>(ldg_hint(rv + j, pol), x);
+      f(x, kEl, j * kEl);
+    }
+  } else {
+    for (int v = tid; v < V; v += NT) {
+      float x[kEl];
+      x[0] = load_logit(row + v);
+      f(x, 1, v);
+    }
+  }
+}
+
 // First bin j of [0, n) (bins run from the largest logits down) at which
 //   by count: the running count through j reaches `need`;
 //   by mass:  cnt[j] > 0 and above + the running mass through j >= bound.
@@ -1322,7 +1358,7 @@ __device__ bool adj_run(const TT* row, int V, bool vec, float M, float c, float 
 // With record, the counted entries' indices and values also go to A.cand;
 // ncand is then their number (every entry at or above x_lo, so every kept
 // one), or -1 when they did not fit (and always -1 without record).
-template <int NT>
+template <int NT, bool kDeep>
 __device__ bool adj_run_keys(const __nv_bfloat16* row, int V, bool vec, float M, float c,
                              float fscale, int top_k, float top_p, bool use_k, bool use_p,
                              unsigned long long s_all, float x_lo, bool record, uint64_t pol,
@@ -1333,7 +1369,7 @@ __device__ bool adj_run_keys(const __nv_bfloat16* row, int V, bool vec, float M,
   for (int j = tid; j < kAdjBins1; j += NT) A.cnt1[j] = 0u;
   if (tid == 0) A.ncand = 0;
   __syncthreads();
-  adj_visit_vec<__nv_bfloat16, NT>(row, V, vec, pol, [&](const float* x, int n, int v0) {
+  auto count = [&](const float* x, int n, int v0) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       if (e < n && x[e] >= x_lo) {
@@ -1346,7 +1382,14 @@ __device__ bool adj_run_keys(const __nv_bfloat16* row, int V, bool vec, float M,
         }
       }
     }
-  });
+  };
+  // rows bounded by the threads' maxima count few entries and need the row
+  // back from DRAM fast (four vectors in flight); the others count many and
+  // keep the smaller loop
+  if constexpr (kDeep)
+    adj_visit_vec4<__nv_bfloat16, NT>(row, V, vec, pol, count);
+  else
+    adj_visit_vec<__nv_bfloat16, NT>(row, V, vec, pol, count);
   __syncthreads();
   ncand = (record && A.ncand <= kAdjCand) ? A.ncand : -1;
   for (int j = tid; j < kAdjBins1; j += NT) {
@@ -1487,7 +1530,7 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
       const int sel = A.sel;
       __syncthreads();
       if (sel < kAdjBins1 - 1) {
-        ok = adj_run_keys<NT>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
+        ok = adj_run_keys<NT, true>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
                               top_k, top_p, use_k, use_p, 0ull, key16_value(ktop - sel), true,
                               pol, A, key, kept, kc, ncand);
         if (ok) adj_count(ctr, kAdjExact);
@@ -1516,7 +1559,7 @@ __device__ __noinline__ bool adjust_row(const TT* row, int V, bool vec, float M,
         }
         if (fin) {
           int nc;
-          ok = adj_run_keys<NT>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
+          ok = adj_run_keys<NT, false>(reinterpret_cast<const __nv_bfloat16*>(row), V, vec, M, c, fscale,
                                 top_k, top_p, use_k, use_p, s_all, x_lo, false, pol, A, key, kept,
                                 kc, nc);
           if (ok) adj_count(ctr, kAdjExact);
