@@ -59,6 +59,14 @@ class Verifier:
         idx = dev.index if dev.index is not None else torch.cuda.current_device()
         rc, self._h = specdec_create(idx)
         _check(rc, "specdec_create")
+        # a valid device address for required arrays that are empty (draft_ids
+        # when every request has gamma = 0): the C ABI wants a pointer even then
+        self._empty = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def _ids_ptr(self, draft_ids) -> int:
+        if draft_ids is not None and draft_ids.numel() == 0:
+            return self._empty.data_ptr()
+        return _ptr(draft_ids)
 
     def close(self):
         if getattr(self, "_h", 0):
@@ -162,21 +170,21 @@ class Verifier:
         stream = _stream_handle(self.device)
         if top_k is not None or top_p is not None:
             rc = specdec_rejection_sample_topk_topp(
-                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),
+                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), self._ids_ptr(draft_ids),
                 _ptr(cu_num_draft_tokens), B, V, float(T), _ptr(top_k), _ptr(top_p), int(seed),
                 int(request_offset), _ptr(out.tokens), _ptr(out.num_accepted), _ptr(out.beta),
                 _ptr(out.target_prob), _ptr(out.draft_prob), _ptr(out.accept), stream)
         elif (out.target_prob is not None or out.draft_prob is not None or out.accept is not None
                 or request_offset):
             rc = specdec_rejection_sample_ex(
-                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),
+                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), self._ids_ptr(draft_ids),
                 _ptr(cu_num_draft_tokens), B, V, float(T), int(seed), int(request_offset),
                 _ptr(out.tokens),
                 _ptr(out.num_accepted), _ptr(out.beta), _ptr(out.target_prob),
                 _ptr(out.draft_prob), _ptr(out.accept), stream)
         else:
             rc = specdec_rejection_sample(
-                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), _ptr(draft_ids),
+                self._h, _ptr(target_logits), dtype, _ptr(draft_probs), self._ids_ptr(draft_ids),
                 _ptr(cu_num_draft_tokens), B, V, float(T), int(seed), _ptr(out.tokens),
                 _ptr(out.num_accepted), _ptr(out.beta), stream)
         _check(rc, "specdec_rejection_sample")

@@ -220,6 +220,19 @@ def test_single_request_bonus_only(V):
     assert g["num_accepted"][0] == 0 and g["tokens"][0] == r.tokens[0]
 
 
+def test_every_request_bonus_only_with_empty_draft_tensors(V):
+    # gamma = 0 for every request: the binding passes empty draft tensors (the
+    # C ABI then gets a valid dummy address for draft_ids); only bonus tokens
+    t = torch.randn(6, 3000, generator=torch.Generator().manual_seed(9)) * 2
+    w = from_rows(t, torch.zeros(0, 3000), torch.zeros(0, dtype=torch.int32), [0] * 6, T=0.8,
+                  seed=17)
+    g = run_gpu(V, w)
+    r = run_oracle(w)
+    st = compare(w, g, r)
+    assert flag_budget_ok(st), st
+    assert (g["num_accepted"] == 0).all()
+
+
 def test_masked_logits_and_zero_draft_probs(V):
     # -inf logits (masked vocabulary) and q(x) = 0 < p(x) (always accepted)
     Vs, gam, B = 2048, 3, 6
